@@ -1,0 +1,325 @@
+"""Benchmark of the NCC hot path on GB300.
+
+One step = the whole path on one 4096x4096 uint8 image and one 16x16 uint8
+template: build both int64 summed-area tables (ncc_sat_build), then the
+numerator and coefficients for all 4081 x 4081 valid shifts (ncc_correlate).
+Prints one JSON line (see the README of the bench contract in the design doc).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank matches its own copy of the image (independent
+problems, no data-path collective): weak scaling, value = all ranks'
+coefficients / the slowest rank's time.  `--impl reference` times the CPU
+oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from normalized_cross_correlation_gb300 import inputs  # noqa: E402
+
+METRIC = "NCC coefficients/s (4096², 16×16 tmpl); SAT build GB/s vs HBM peak"
+UNIT = "coefficients/s"
+SAT_BYTES_PER_PX = 17          # 1 B read + 8 B (S) + 8 B (Q) written per pixel
+CORR_BYTES_PER_COEFF = 21      # S and Q corners (16 B after reuse) + 1 B image + 4 B out
+L2_FLUSH_BYTES = 512 << 20     # > 129 MB L2
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0,
+            "source": "fallback"}
+
+
+# Integer dot-product pipe: dp4a instructions per SM per clock on sm_103a,
+# measured by a throughput microbenchmark (see the design notes); the ALU
+# roofline is this times 152 SMs times the maximum SM clock.
+DP4A_PER_SM_CLK = 64
+N_SMS = 152
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"ncc_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self) -> dict:
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [v for v in sm if v >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def oracle_sample_rate(w: inputs.Workload, band_rows: int, threads: int) -> tuple[float, float]:
+    """Times the CPU oracle on the top band of the workload: the tables of the
+    band's image rows plus every coefficient of `band_rows` output rows.
+    Returns (coefficients per second, seconds)."""
+    import oracle
+    sub = np.ascontiguousarray(w.image[: band_rows + w.hT - 1])
+    t0 = time.perf_counter()
+    oracle.sat(sub)
+    oracle.correlate(sub, w.templates, threads=threads)
+    dt = time.perf_counter() - t0
+    return band_rows * w.Ox / dt, dt
+
+
+def run_reference(args, w: inputs.Workload) -> dict:
+    import oracle
+    threads = oracle.default_threads()
+    band = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample_rate(w, band, threads)
+    times = []
+    for _ in range(args.steps):
+        _, dt = oracle_sample_rate(w, band, threads)
+        times.append(dt)
+    per_step = statistics.mean(times)
+    rate = band * w.Ox / per_step
+    sample = (f"tables of the top {band + w.hT - 1} image rows + all {band}x{w.Ox} "
+              f"coefficients of those rows, per step")
+    return {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": w.name, "image": "4096x4096 u8", "template": "16x16 u8",
+                   "sample_rows": band},
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_gpu(args, w: inputs.Workload) -> dict | None:
+    import torch
+    from normalized_cross_correlation_gb300 import ncc
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    ncc.lib()
+    stream = torch.cuda.current_stream()
+    dev = torch.device("cuda", local)
+
+    img = torch.from_numpy(w.image).to(dev)
+    tmpl = torch.from_numpy(w.templates[0]).to(dev)
+    S = torch.empty((w.H, w.W), dtype=torch.int64, device=dev)
+    Q = torch.empty((w.H, w.W), dtype=torch.int64, device=dev)
+    out = torch.empty((w.Oy, w.Ox), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    L = ncc.lib()
+    sh = stream.cuda_stream
+
+    def step():
+        rc = L.ncc_sat_build(img.data_ptr(), w.W, w.H, S.data_ptr(), Q.data_ptr(), sh)
+        assert rc == 0, rc
+        ev_mid.record(stream)
+        rc = L.ncc_correlate(img.data_ptr(), w.W, w.H, tmpl.data_ptr(), w.wT, w.hT,
+                             S.data_ptr(), Q.data_ptr(), out.data_ptr(), sh)
+        assert rc == 0, rc
+
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_m = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_mid = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert ncc.ncc_sync_status() == 0
+
+    clocks = ClockSampler(local)
+    with clocks:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for k in range(args.steps):
+            flush.zero_()                       # L2 flushed between timed steps
+            ev_a[k].record(stream)
+            ev_mid = ev_m[k]
+            step()
+            ev_b[k].record(stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+    assert ncc.ncc_sync_status() == 0
+    t_sat = [ev_a[k].elapsed_time(ev_m[k]) for k in range(args.steps)]
+    t_corr = [ev_m[k].elapsed_time(ev_b[k]) for k in range(args.steps)]
+    t_step = [a + b for a, b in zip(t_sat, t_corr)]
+    ms_step = statistics.mean(t_step)
+    if dist is not None:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    coeffs = w.Ox * w.Oy
+    value = ws * coeffs / (ms_step * 1e-3)
+
+    # end to end through the host-buffer entry point (pinned host memory)
+    himg = torch.from_numpy(w.image).pin_memory()
+    htmp = torch.from_numpy(w.templates).pin_memory()
+    hout = torch.empty((1, w.Oy, w.Ox), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        ncc.ncc_match_host(himg, htmp, hout)
+    e2e_t = []
+    for _ in range(e2e_steps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ncc.ncc_match_host(himg, htmp, hout)      # synchronizes the stream
+        e2e_t.append(time.perf_counter() - t0)
+    e2e_ms = statistics.mean(e2e_t) * 1e3
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    peaks = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    sat_ms, corr_ms = statistics.mean(t_sat), statistics.mean(t_corr)
+    sat_gbs = SAT_BYTES_PER_PX * w.W * w.H / (sat_ms * 1e-3) / 1e9
+    corr_gbs = CORR_BYTES_PER_COEFF * coeffs / (corr_ms * 1e-3) / 1e9
+    dp4a = coeffs * ((w.wT + 3) // 4) * w.hT
+    alu_peak = DP4A_PER_SM_CLK * N_SMS * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+    roof_sat = {"kernel": "sat_build", "bound": "hbm", "achieved": sat_gbs, "peak": hbm,
+                "unit": "GB/s", "frac": sat_gbs / hbm, "traffic": None,
+                "peak_source": peaks["source"]}
+    roof_corr_alu = {"kernel": "corr_dp4a", "bound": "alu", "achieved": dp4a / (corr_ms * 1e-3) / 1e12,
+                     "peak": alu_peak / 1e12, "unit": "Tdp4a/s",
+                     "frac": dp4a / (corr_ms * 1e-3) / alu_peak, "traffic": None}
+    roof_corr_hbm = {"kernel": "corr_dp4a", "bound": "hbm", "achieved": corr_gbs, "peak": hbm,
+                     "unit": "GB/s", "frac": corr_gbs / hbm, "traffic": None}
+    corr_roof = max(roof_corr_alu, roof_corr_hbm, key=lambda r: r["frac"])
+    dominant = roof_sat if sat_ms >= corr_ms else corr_roof
+
+    cpu = None
+    if args.cpu_baseline:
+        import oracle
+        threads = oracle.default_threads()
+        rate, dt = oracle_sample_rate(w, args.ref_rows, threads)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"tables of the top {args.ref_rows + w.hT - 1} image rows + all "
+                         f"{args.ref_rows}x{w.Ox} coefficients of those rows ({dt:.1f} s)"}
+
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": w.name, "image": "4096x4096 u8 uniform (seed 2)",
+                   "template": "16x16 u8 crop", "step": "ncc_sat_build + ncc_correlate",
+                   "l2": "flushed between timed steps (512 MB write)"},
+        "sat_build": {"ms": sat_ms, "GB/s": sat_gbs, "frac_of_hbm": sat_gbs / hbm},
+        "correlate": {"ms": corr_ms, "GB/s": corr_gbs, "Tdp4a/s": roof_corr_alu["achieved"],
+                      "GMAC/s": coeffs * w.wT * w.hT / (corr_ms * 1e-3) / 1e9},
+        "roofline": {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")},
+        "rooflines": [roof_sat, roof_corr_hbm, roof_corr_alu],
+        "cpu_baseline": cpu,
+        "e2e": {"value": ws * coeffs / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": int(w.image.nbytes + w.templates.nbytes),
+                "d2h_bytes_per_step": int(coeffs * 4)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=4081,
+                    help="output rows of the oracle's bounded sample per step")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "gb300" else args.warmup
+
+    w = inputs.headline_4096()
+    ws, rank, _ = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, w)), flush=True)
+        return
+    res = run_gpu(args, w)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

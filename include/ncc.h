@@ -1,0 +1,165 @@
+/*
+ * ncc.h -- C ABI of the GB300 (sm_103a) normalized cross-correlation library.
+ *
+ * Normalized cross-correlation (NCC) template matching of an 8-bit image
+ * against 8-bit templates, after The CUDA Handbook, chapter 15 ("Image
+ * Processing: Normalized Correlation"):
+ *   - the denominators' first and second moments come from two inclusive
+ *     int64 summed-area tables, S of I and Q of I^2, read with the
+ *     four-corner box sum (section 15.8, "The Denominator: Summed Area
+ *     Tables", Figure 15-7);
+ *   - the numerator SumIT is swept over every valid shift and combined with
+ *     the moments into one coefficient per shift ("Image in shared memory",
+ *     Listing 15-5).
+ *
+ * Coefficient (the listing names the routine but does not print its body;
+ * this library takes Pearson's correlation in exact-integer form):
+ *     N   = wT*hT
+ *     num = N*SumIT - SumI*SumT
+ *     vI  = N*SumI2 - SumI^2,    vT = N*SumT2 - SumT^2
+ *     r   = num / sqrt(vI*vT)    (0 when vI == 0 or vT == 0; clamped to [-1,1])
+ * num, vI and vT are exact 64-bit integers; r is rounded to fp32.
+ *
+ * Conventions shared by every entry point:
+ *   - Images are dense row-major uint8 [H][W] (row stride W bytes).
+ *     Templates are dense uint8 [nT][hT][wT].  Tables are dense int64 [H][W].
+ *   - Valid shifts only: Ox = W-wT+1 columns, Oy = H-hT+1 rows.  Coefficient
+ *     maps are dense fp32 [nT][Oy][Ox]; out[t][y][x] belongs to the window of
+ *     template t whose top-left image pixel is (x, y).
+ *   - Unless an entry point says otherwise, every pointer is a DEVICE pointer
+ *     owned by the caller.  The library never frees caller memory and keeps
+ *     no reference to it after the call returns.
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) on the current CUDA device.  The return
+ *     value covers argument checks, workspace allocation and launch errors
+ *     only.  Errors found by a kernel while it runs (a look-back wait that
+ *     ran out) are recorded in a per-device status word and reported by
+ *     ncc_sync_status().
+ *   - Limits: 1 <= W <= 66051 (a row's running sum of squares must fit in
+ *     uint32: 66051 * 255^2 < 2^32), 1 <= H, W*H < 2^31, and
+ *     wT*hT <= 66051 (the numerator is accumulated in uint32).  Larger
+ *     inputs return NCC_ERR_UNSUPPORTED rather than wrong results.
+ */
+#ifndef NCC_GB300_H
+#define NCC_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *ncc_stream_t;
+
+/* Status codes (0 = success, negative = failure). */
+enum ncc_status_code {
+    NCC_OK = 0,
+    NCC_ERR_INVALID_ARG = -1,  /* null/misaligned pointer, bad size, aliasing  */
+    NCC_ERR_UNSUPPORTED = -2,  /* valid request outside the library's limits  */
+    NCC_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed         */
+    NCC_ERR_TIMEOUT = -4,      /* a kernel's bounded wait ran out (device)     */
+    NCC_ERR_NOMEM = -5         /* stream-ordered workspace allocation failed   */
+};
+
+/*
+ * ncc_sat_build -- the two summed-area tables of section 15.8.
+ *   S[y][x] = sum_{j<=y, i<=x} I[j][i],  Q[y][x] = sum_{j<=y, i<=x} I[j][i]^2
+ * (inclusive; int64 because the totals pass 2^31 by a 512x512 image; each
+ * row's running sums fit uint32, as the section notes).
+ *   img  device, uint8 [H][W], read only.
+ *   S, Q device, int64 [H][W], written completely; 8-byte aligned; must not
+ *        overlap each other or img.
+ * Single pass: a decoupled look-back scan over tiles, handed out in
+ * row-major order so that every wait points at an earlier tile.  Uses a
+ * stream-ordered workspace (cudaMallocAsync/cudaFreeAsync on `stream`).
+ * Returns NCC_OK, NCC_ERR_INVALID_ARG, NCC_ERR_UNSUPPORTED, NCC_ERR_NOMEM or
+ * NCC_ERR_CUDA.
+ */
+int ncc_sat_build(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
+                  ncc_stream_t stream);
+
+/*
+ * ncc_correlate -- one template, every valid shift (Listing 15-5's sums,
+ * section 15.8's box sums, the coefficient above).
+ *   img  device uint8 [H][W].
+ *   tmpl device uint8 [hT][wT].
+ *   S, Q device int64 [H][W]: must hold ncc_sat_build(img) output, ordered
+ *        before this call (same stream, or an event).
+ *   out  device fp32 [Oy][Ox], written completely; must not overlap inputs.
+ * Returns NCC_OK, NCC_ERR_INVALID_ARG, NCC_ERR_UNSUPPORTED or NCC_ERR_CUDA.
+ */
+int ncc_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl,
+                  int wT, int hT, const int64_t *S, const int64_t *Q,
+                  float *out, ncc_stream_t stream);
+
+/*
+ * ncc_correlate_bank -- nT templates of one size against one image; one SAT
+ * pair serves every template of the bank (section 15.8).
+ *   tmpl device uint8 [nT][hT][wT];  out device fp32 [nT][Oy][Ox].
+ *   Other arguments as ncc_correlate.  1 <= nT.
+ * Returns as ncc_correlate.
+ */
+int ncc_correlate_bank(const uint8_t *img, int W, int H, const uint8_t *tmpl,
+                       int wT, int hT, int nT, const int64_t *S,
+                       const int64_t *Q, float *out, ncc_stream_t stream);
+
+/*
+ * ncc_correlate_moments -- the exact integer sums behind the coefficients,
+ * for verification: per shift SumI and SumI2 (from S and Q by the
+ * four-corner box sum) and per template and shift SumIT (Listing 15-5).
+ *   sumI, sumI2 device int64 [Oy][Ox];  sumIT device int64 [nT][Oy][Ox].
+ *   Other arguments as ncc_correlate_bank; the same kernels compute the
+ *   numerator as in ncc_correlate (nT == 1) or ncc_correlate_bank (nT > 1).
+ * Returns as ncc_correlate.
+ */
+int ncc_correlate_moments(const uint8_t *img, int W, int H,
+                          const uint8_t *tmpl, int wT, int hT, int nT,
+                          const int64_t *S, const int64_t *Q, int64_t *sumI,
+                          int64_t *sumI2, int64_t *sumIT, ncc_stream_t stream);
+
+/*
+ * ncc_match_host -- the whole path with HOST buffers: copies img and tmpl to
+ * the device, builds S and Q, correlates every template and copies the
+ * coefficients back, all ordered on `stream`, then synchronizes it.
+ *   img  host uint8 [H][W];  tmpl host uint8 [nT][hT][wT];
+ *   out  host fp32 [nT][Oy][Ox].  Page-locked host memory makes the copies
+ *   asynchronous and fast; pageable memory also works.
+ * Device buffers come from cudaMallocAsync on `stream` and are released
+ * before return.  Returns the first failure among the steps, including any
+ * status recorded by the kernels (as ncc_sync_status would).
+ */
+int ncc_match_host(const uint8_t *img, int W, int H, const uint8_t *tmpl,
+                   int wT, int hT, int nT, float *out, ncc_stream_t stream);
+
+/*
+ * ncc_sync_status -- synchronizes `stream`, then returns and clears the
+ * current device's status word: NCC_OK, or the first error a kernel
+ * recorded since the last call (NCC_ERR_TIMEOUT when a look-back wait ran
+ * out).  The word is per device, shared by all streams on it.  Returns
+ * NCC_ERR_CUDA if the synchronization itself fails.
+ */
+int ncc_sync_status(ncc_stream_t stream);
+
+/* Static, human-readable text for a status code. */
+const char *ncc_status_string(int status);
+
+/* Library version, (major << 16) | minor. */
+int ncc_version(void);
+
+/*
+ * ncc_debug_set_fault -- test hook for the bounded waits.  While
+ * suppress_tile >= 0, the SAT builder's tile with that row-major index never
+ * publishes its look-back results, so every tile that depends on it waits
+ * until its limit (timeout_ns; 0 restores the default of one second) runs
+ * out and records NCC_ERR_TIMEOUT.  suppress_tile = -1 restores normal
+ * operation.  Process-wide; not for concurrent use.
+ */
+int ncc_debug_set_fault(int suppress_tile, uint64_t timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NCC_GB300_H */

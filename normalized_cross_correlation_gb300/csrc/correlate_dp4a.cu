@@ -1,0 +1,345 @@
+// correlate_dp4a.cu -- one template against every valid shift of an 8-bit
+// image, with the numerator on the integer dot-product pipe (__dp4a) and a
+// fused epilogue that reads the window moments from the summed-area tables
+// and writes the fp32 coefficient.
+//
+// Follows The CUDA Handbook, chapter 15: "Image in shared memory"
+// (Listing 15-5: the image tile plus a template-sized overfetch is staged in
+// shared memory and each thread sums I*T over its windows), and section 15.8
+// (SumI and SumI2 of every window from S and Q by the four-corner box sum).
+//
+// GB300 design:
+//   - Output tile: 128 shifts wide by 32 rows; 256 threads; each thread owns
+//     4 rows x 4 shifts.  Lane = 4*qg + d owns the shifts x0 + 16*qg + 4*k + d
+//     (k = 0..3).
+//   - The tile plus its (wT-1) x (hT-1) halo is one TMA box (cp.async.bulk.
+//     tensor, completion on an mbarrier).  Images whose rows are not a
+//     multiple of 16 bytes fall back to plain loads.
+//   - Four byte-shifted copies of the staged tile (copy d starts d bytes
+//     later) let every lane read 32-bit-aligned groups of four pixels for its
+//     phase d, so the inner loop is two 16-byte shared loads per image row and
+//     template chunk plus 16 __dp4a per output row -- no byte permutes.  The
+//     copies sit 32 bytes (mod 128) apart so the eight lanes of each shared
+//     load phase hit distinct banks.
+//   - The template is packed into 32-bit words in shared memory, in chunks of
+//     16 pixels, zero-padded to a multiple of 16 (the zero bytes cancel any
+//     pixels read past the window).
+//   - SumIT accumulates in uint32 (exact while wT*hT*255^2 < 2^32).
+#include "ncc_common.cuh"
+
+#include <cuda.h>
+#include <math.h>
+
+namespace ncc {
+namespace {
+
+constexpr int kOutW = 128;
+constexpr int kRowsPerThread = 4;
+constexpr int kWarps = 8;
+constexpr int kOutH = kWarps * kRowsPerThread;
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxTmaBox = 256;        // TMA box extent limit per dimension
+constexpr int kMaxSmem = 227 * 1024;   // opt-in shared memory per CTA
+
+struct Geom {
+    int nch;         // 16-pixel template chunks
+    int boxW;        // staged tile width in bytes = kOutW + 16*nch
+    int boxH;        // staged tile height = kOutH + hT - 1
+    int copyStride;  // bytes between shifted copies
+    int tmplOff;     // offset of the packed template
+    int smemBytes;   // dynamic shared memory (plus 128 bytes of alignment slack)
+};
+
+Geom make_geom(int wT, int hT) {
+    Geom g;
+    g.nch = (wT + 15) / 16;
+    g.boxW = kOutW + 16 * g.nch;
+    g.boxH = kOutH + hT - 1;
+    const int copyBytes = g.boxW * g.boxH;
+    g.copyStride = (copyBytes + 127) / 128 * 128 + 32;
+    g.tmplOff = 4 * g.copyStride;
+    g.smemBytes = g.tmplOff + hT * g.nch * 16 + 128;
+    return g;
+}
+
+struct KParams {
+    const uint8_t *img;
+    int W, H;
+    const uint8_t *tmpl;
+    int wT, hT;
+    const long long *S, *Q;
+    float *out;
+    long long *sumI, *sumI2, *sumIT;
+    int *status;
+    int Ox, Oy;
+    Geom g;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ long long box_sum(const long long *__restrict__ T, int W, int x, int y,
+                                             int w, int h) {
+    // four-corner rule over [x, x+w) x [y, y+h); row -1 / column -1 read as 0
+    const int xr = x + w - 1, yb = y + h - 1;
+    long long v = __ldg(&T[(size_t)yb * W + xr]);
+    if (y > 0) v -= __ldg(&T[(size_t)(y - 1) * W + xr]);
+    if (x > 0) v -= __ldg(&T[(size_t)yb * W + (x - 1)]);
+    if (x > 0 && y > 0) v += __ldg(&T[(size_t)(y - 1) * W + (x - 1)]);
+    return v;
+}
+
+template <bool kTma, bool kMoments>
+__global__ void __launch_bounds__(kThreads)
+corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const KParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    __shared__ __align__(8) unsigned long long s_bar;
+    __shared__ long long s_red[kWarps][2];
+    __shared__ long long s_sumT;
+    __shared__ long long s_vT;
+    __shared__ float s_invSqrtVT;
+
+    const Geom &g = p.g;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int x0 = blockIdx.x * kOutW, y0 = blockIdx.y * kOutH;
+
+    // --- stage the image tile (copy 0) ---------------------------------
+    if (kTma) {
+        if (tid == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar)));
+            asm volatile("fence.mbarrier_init.release.cluster;");
+            asm volatile("fence.proxy.async.shared::cta;");
+            const uint32_t bytes = (uint32_t)(g.boxW * g.boxH);
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                         ::"r"(smem_u32(&s_bar)), "r"(bytes) : "memory");
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                " [%0], [%1, {%2, %3}], [%4];"
+                ::"r"(smem_u32(smem)), "l"(&tmap), "r"(x0), "r"(y0), "r"(smem_u32(&s_bar))
+                : "memory");
+        }
+    } else {
+        for (int idx = tid; idx < g.boxW * g.boxH; idx += kThreads) {
+            const int r = idx / g.boxW, c = idx - r * g.boxW;
+            const int y = y0 + r, x = x0 + c;
+            smem[idx] = (y < p.H && x < p.W) ? __ldg(p.img + (size_t)y * p.W + x) : (uint8_t)0;
+        }
+    }
+
+    // --- pack the template, template statistics (overlaps the TMA) -------
+    uint32_t *tw = reinterpret_cast<uint32_t *>(smem + g.tmplOff);
+    const int nWords = p.hT * g.nch * 4;
+    for (int wi = tid; wi < nWords; wi += kThreads) {
+        const int j = wi / (g.nch * 4), cw = wi - j * g.nch * 4;
+        uint32_t v = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const int i = 4 * cw + b;
+            if (i < p.wT) v |= (uint32_t)__ldg(p.tmpl + (size_t)j * p.wT + i) << (8 * b);
+        }
+        tw[wi] = v;
+    }
+    {
+        long long a = 0, b = 0;
+        for (int i = tid; i < p.wT * p.hT; i += kThreads) {
+            const long long t = __ldg(p.tmpl + i);
+            a += t;
+            b += t * t;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, o);
+            b += __shfl_xor_sync(0xffffffffu, b, o);
+        }
+        if (lane == 0) { s_red[warp][0] = a; s_red[warp][1] = b; }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        long long a = 0, b = 0;
+        for (int w = 0; w < kWarps; ++w) { a += s_red[w][0]; b += s_red[w][1]; }
+        const long long N = (long long)p.wT * p.hT;
+        s_sumT = a;
+        s_vT = N * b - a * a;
+        s_invSqrtVT = s_vT > 0 ? (float)(1.0 / sqrt((double)s_vT)) : 0.0f;
+    }
+    if (kTma) {
+        // every thread waits for the TMA transaction to land
+        uint32_t done = 0;
+        for (unsigned it = 0; !done; ++it) {
+            asm volatile(
+                "{ .reg .pred P; mbarrier.try_wait.parity.shared::cta.b64 P, [%1], 0; selp.u32 %0, 1, 0, P; }"
+                : "=r"(done) : "r"(smem_u32(&s_bar)) : "memory");
+            if (it > (1u << 24)) {        // a TMA that never lands is reported, never a hang
+                record_status(p.status, NCC_ERR_TIMEOUT);
+                break;
+            }
+        }
+    }
+    __syncthreads();
+
+    // --- byte-shifted copies 1..3 -----------------------------------------
+    {
+        const uint32_t *c0 = reinterpret_cast<const uint32_t *>(smem);
+        const int words = (g.boxW * g.boxH) / 4;
+        for (int wi = tid; wi < words; wi += kThreads) {
+            const uint32_t lo = c0[wi], hi = c0[wi + 1];  // c0[words] is padding: only meets zero template bytes
+            reinterpret_cast<uint32_t *>(smem + 1 * g.copyStride)[wi] = __byte_perm(lo, hi, 0x4321);
+            reinterpret_cast<uint32_t *>(smem + 2 * g.copyStride)[wi] = __byte_perm(lo, hi, 0x5432);
+            reinterpret_cast<uint32_t *>(smem + 3 * g.copyStride)[wi] = __byte_perm(lo, hi, 0x6543);
+        }
+    }
+    __syncthreads();
+
+    // --- numerator: SumIT for 4 rows x 4 shifts per thread -----------------
+    const int qg = lane >> 2, d = lane & 3;
+    const uint8_t *cp = smem + d * g.copyStride + 16 * qg;
+    uint32_t acc[kRowsPerThread][4];
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[i][k] = 0u;
+
+    const int rows = kRowsPerThread + p.hT - 1;
+    for (int c = 0; c < g.nch; ++c) {
+        const uint8_t *cc = cp + 16 * c;
+        const uint4 *tc = reinterpret_cast<const uint4 *>(tw) + c;  // chunk c of row j at tc[j*nch]
+        for (int r = 0; r < rows; ++r) {
+            const uint8_t *rp = cc + (warp * kRowsPerThread + r) * g.boxW;
+            const uint4 a = *reinterpret_cast<const uint4 *>(rp);
+            const uint4 b = *reinterpret_cast<const uint4 *>(rp + 16);
+            const uint32_t v[7] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z};
+#pragma unroll
+            for (int i = 0; i < kRowsPerThread; ++i) {
+                const int j = r - i;
+                if (j >= 0 && j < p.hT) {
+                    const uint4 t = tc[j * g.nch];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t s = acc[i][k];
+                        s = __dp4a(v[k + 0], t.x, s);
+                        s = __dp4a(v[k + 1], t.y, s);
+                        s = __dp4a(v[k + 2], t.z, s);
+                        s = __dp4a(v[k + 3], t.w, s);
+                        acc[i][k] = s;
+                    }
+                }
+            }
+        }
+    }
+
+    // --- epilogue: moments from S and Q, coefficient -----------------------
+    const long long N = (long long)p.wT * p.hT;
+    const long long sT = s_sumT, vT = s_vT;
+    const float invSqrtVT = s_invSqrtVT;
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i) {
+        const int y = y0 + warp * kRowsPerThread + i;
+        if (y >= p.Oy) break;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int x = x0 + 16 * qg + 4 * k + d;
+            if (x >= p.Ox) continue;
+            const long long sI = box_sum(p.S, p.W, x, y, p.wT, p.hT);
+            const long long sI2 = box_sum(p.Q, p.W, x, y, p.wT, p.hT);
+            const size_t o = (size_t)y * p.Ox + x;
+            if (kMoments) {
+                p.sumI[o] = sI;
+                p.sumI2[o] = sI2;
+                p.sumIT[o] = (long long)acc[i][k];
+            } else {
+                const long long num = N * (long long)acc[i][k] - sI * sT;
+                const long long vI = N * sI2 - sI * sI;
+                float r = 0.0f;
+                if (vI > 0 && vT > 0) {
+                    r = (float)num * rsqrtf((float)vI) * invSqrtVT;
+                    r = fminf(1.0f, fmaxf(-1.0f, r));
+                }
+                __stcs(p.out + o, r);
+            }
+        }
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+}  // namespace
+
+bool corr_dp4a_supported(int wT, int hT) {
+    return wT >= 1 && hT >= 1 && make_geom(wT, hT).smemBytes <= kMaxSmem;
+}
+
+cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
+    KParams p;
+    p.img = a.img; p.W = a.W; p.H = a.H;
+    p.tmpl = a.tmpl; p.wT = a.wT; p.hT = a.hT;
+    p.S = reinterpret_cast<const long long *>(a.S);
+    p.Q = reinterpret_cast<const long long *>(a.Q);
+    p.out = a.out;
+    p.sumI = reinterpret_cast<long long *>(a.sumI);
+    p.sumI2 = reinterpret_cast<long long *>(a.sumI2);
+    p.sumIT = reinterpret_cast<long long *>(a.sumIT);
+    p.status = a.status;
+    p.Ox = a.W - a.wT + 1;
+    p.Oy = a.H - a.hT + 1;
+    p.g = make_geom(a.wT, a.hT);
+
+    CUtensorMap tmap;
+    memset(&tmap, 0, sizeof(tmap));
+    bool tma = (a.W % 16 == 0) && ((uintptr_t)a.img % 16 == 0) && p.g.boxW <= kMaxTmaBox &&
+               p.g.boxH <= kMaxTmaBox;
+    EncodeTiledFn enc = tma ? encode_fn() : nullptr;
+    if (enc) {
+        const cuuint64_t dims[2] = {(cuuint64_t)a.W, (cuuint64_t)a.H};
+        const cuuint64_t strides[1] = {(cuuint64_t)a.W};
+        const cuuint32_t box[2] = {(cuuint32_t)p.g.boxW, (cuuint32_t)p.g.boxH};
+        const cuuint32_t estr[2] = {1, 1};
+        CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.img), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        tma = (r == CUDA_SUCCESS);
+    } else {
+        tma = false;
+    }
+    const bool moments = a.sumIT != nullptr;
+    const dim3 grid((p.Ox + kOutW - 1) / kOutW, (p.Oy + kOutH - 1) / kOutH);
+    const dim3 block(kThreads);
+    const size_t smem = (size_t)p.g.smemBytes;
+    cudaError_t e;
+#define NCC_LAUNCH(T, M)                                                                     \
+    do {                                                                                     \
+        e = cudaFuncSetAttribute(corr_dp4a_kernel<T, M>,                                     \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);    \
+        if (e != cudaSuccess) return e;                                                      \
+        corr_dp4a_kernel<T, M><<<grid, block, smem, stream>>>(tmap, p);                      \
+    } while (0)
+    if (tma && moments) NCC_LAUNCH(true, true);
+    else if (tma) NCC_LAUNCH(true, false);
+    else if (moments) NCC_LAUNCH(false, true);
+    else NCC_LAUNCH(false, false);
+#undef NCC_LAUNCH
+    return cudaGetLastError();
+}
+
+}  // namespace ncc

@@ -1,0 +1,243 @@
+// ncc_api.cu -- the library's C ABI (declared in include/ncc.h): argument
+// checks, stream-ordered workspace, kernel selection and the per-device
+// status word.
+#include "ncc_common.cuh"
+
+#include <mutex>
+#include <string.h>
+
+namespace {
+
+// Per-device status word written by kernels (first error wins).
+__device__ int g_ncc_status = 0;
+
+constexpr int kMaxDevices = 64;
+int *g_status_ptr[kMaxDevices] = {};
+std::mutex g_mutex;
+
+// Test hook state (ncc_debug_set_fault).
+int g_fault_tile = -1;
+uint64_t g_timeout_ns = 1000000000ull;
+
+constexpr int kMaxW = 66051;  // 66051 * 255^2 < 2^32: a row's running sum of squares fits uint32
+constexpr long long kMaxN = 66051;  // wT*hT*255^2 < 2^32: SumIT fits uint32
+
+int status_ptr(int **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NCC_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ncc_status) != cudaSuccess) return NCC_ERR_CUDA;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    *out = g_status_ptr[dev];
+    return NCC_OK;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const char *pa = static_cast<const char *>(a), *pb = static_cast<const char *>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+int check_image(const uint8_t *img, int W, int H) {
+    if (!img || W <= 0 || H <= 0) return NCC_ERR_INVALID_ARG;
+    if (W > kMaxW || (long long)W * H >= (1ll << 31)) return NCC_ERR_UNSUPPORTED;
+    return NCC_OK;
+}
+
+int check_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT,
+                    int nT, const int64_t *S, const int64_t *Q) {
+    int rc = check_image(img, W, H);
+    if (rc != NCC_OK) return rc;
+    if (!tmpl || !S || !Q || wT < 1 || hT < 1 || nT < 1 || wT > W || hT > H)
+        return NCC_ERR_INVALID_ARG;
+    if ((uintptr_t)S % 8 || (uintptr_t)Q % 8) return NCC_ERR_INVALID_ARG;
+    if ((long long)wT * hT > kMaxN) return NCC_ERR_UNSUPPORTED;
+    if ((long long)nT * (W - wT + 1) * (long long)(H - hT + 1) >= (1ll << 40))
+        return NCC_ERR_UNSUPPORTED;
+    return NCC_OK;
+}
+
+int to_status(cudaError_t e) {
+    if (e == cudaSuccess) return NCC_OK;
+    if (e == cudaErrorMemoryAllocation) return NCC_ERR_NOMEM;
+    return NCC_ERR_CUDA;
+}
+
+// Numerator + epilogue for nT templates, either coefficients or moments.
+int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT, int nT,
+                  const int64_t *S, const int64_t *Q, float *out, int64_t *sumI,
+                  int64_t *sumI2, int64_t *sumIT, cudaStream_t stream) {
+    int *status = nullptr;
+    int rc = status_ptr(&status);
+    if (rc != NCC_OK) return rc;
+    const size_t Ox = (size_t)(W - wT + 1), Oy = (size_t)(H - hT + 1);
+    const size_t plane = Ox * Oy;
+    if (nT > 1 && ncc::bank_tc_supported(W, H, wT, hT, nT)) {
+        ncc::BankArgs b{img, W, H, tmpl, wT, hT, nT, S, Q, out, sumI, sumI2, sumIT, status};
+        return to_status(ncc::bank_tc_launch(b, stream));
+    }
+    if (!ncc::corr_dp4a_supported(wT, hT)) return NCC_ERR_UNSUPPORTED;
+    for (int t = 0; t < nT; ++t) {
+        ncc::CorrArgs a;
+        a.img = img; a.W = W; a.H = H;
+        a.tmpl = tmpl + (size_t)t * wT * hT;
+        a.wT = wT; a.hT = hT; a.S = S; a.Q = Q;
+        a.out = out ? out + (size_t)t * plane : nullptr;
+        // the window moments do not depend on the template; every launch
+        // rewrites the same SumI/SumI2 plane
+        a.sumI = sumI;
+        a.sumI2 = sumI2;
+        a.sumIT = sumIT ? sumIT + (size_t)t * plane : nullptr;
+        a.status = status;
+        cudaError_t e = ncc::corr_dp4a_launch(a, stream);
+        if (e != cudaSuccess) return to_status(e);
+    }
+    return NCC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ncc_sat_build(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
+                  ncc_stream_t stream) {
+    int rc = check_image(img, W, H);
+    if (rc != NCC_OK) return rc;
+    if (!S || !Q || (uintptr_t)S % 8 || (uintptr_t)Q % 8) return NCC_ERR_INVALID_ARG;
+    const size_t n = (size_t)W * H;
+    if (overlaps(S, n * 8, Q, n * 8) || overlaps(S, n * 8, img, n) || overlaps(Q, n * 8, img, n))
+        return NCC_ERR_INVALID_ARG;
+    int *status = nullptr;
+    rc = status_ptr(&status);
+    if (rc != NCC_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const ncc::SatPlan plan = ncc::sat_plan(W, H);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, plan.total_bytes, st);
+    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? NCC_ERR_NOMEM : NCC_ERR_CUDA;
+    e = cudaMemsetAsync(ws, 0, plan.zero_bytes, st);
+    if (e == cudaSuccess) {
+        int fault;
+        uint64_t timeout;
+        {
+            std::lock_guard<std::mutex> lock(g_mutex);
+            fault = g_fault_tile;
+            timeout = g_timeout_ns;
+        }
+        e = ncc::sat_launch(img, W, H, S, Q, ws, plan, status, timeout, fault, st);
+    }
+    cudaError_t ef = cudaFreeAsync(ws, st);
+    if (e != cudaSuccess) return to_status(e);
+    return to_status(ef);
+}
+
+int ncc_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT,
+                  const int64_t *S, const int64_t *Q, float *out, ncc_stream_t stream) {
+    return ncc_correlate_bank(img, W, H, tmpl, wT, hT, 1, S, Q, out, stream);
+}
+
+int ncc_correlate_bank(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT,
+                       int nT, const int64_t *S, const int64_t *Q, float *out,
+                       ncc_stream_t stream) {
+    int rc = check_correlate(img, W, H, tmpl, wT, hT, nT, S, Q);
+    if (rc != NCC_OK) return rc;
+    if (!out || (uintptr_t)out % 4) return NCC_ERR_INVALID_ARG;
+    const size_t n = (size_t)W * H;
+    const size_t nout = (size_t)nT * (W - wT + 1) * (H - hT + 1) * sizeof(float);
+    if (overlaps(out, nout, S, n * 8) || overlaps(out, nout, Q, n * 8) ||
+        overlaps(out, nout, img, n) || overlaps(out, nout, tmpl, (size_t)nT * wT * hT))
+        return NCC_ERR_INVALID_ARG;
+    return run_correlate(img, W, H, tmpl, wT, hT, nT, S, Q, out, nullptr, nullptr, nullptr,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ncc_correlate_moments(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT,
+                          int nT, const int64_t *S, const int64_t *Q, int64_t *sumI,
+                          int64_t *sumI2, int64_t *sumIT, ncc_stream_t stream) {
+    int rc = check_correlate(img, W, H, tmpl, wT, hT, nT, S, Q);
+    if (rc != NCC_OK) return rc;
+    if (!sumI || !sumI2 || !sumIT || (uintptr_t)sumI % 8 || (uintptr_t)sumI2 % 8 ||
+        (uintptr_t)sumIT % 8)
+        return NCC_ERR_INVALID_ARG;
+    const size_t plane = (size_t)(W - wT + 1) * (H - hT + 1) * 8;
+    if (overlaps(sumI, plane, sumI2, plane) || overlaps(sumI, plane, sumIT, plane * nT) ||
+        overlaps(sumI2, plane, sumIT, plane * nT))
+        return NCC_ERR_INVALID_ARG;
+    return run_correlate(img, W, H, tmpl, wT, hT, nT, S, Q, nullptr, sumI, sumI2, sumIT,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ncc_match_host(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT,
+                   int nT, float *out, ncc_stream_t stream) {
+    int rc = check_image(img, W, H);
+    if (rc != NCC_OK) return rc;
+    if (!tmpl || !out || wT < 1 || hT < 1 || nT < 1 || wT > W || hT > H)
+        return NCC_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t n = (size_t)W * H, nt = (size_t)nT * wT * hT;
+    const size_t nout = (size_t)nT * (W - wT + 1) * (H - hT + 1);
+    // one device block: tables first (8-byte aligned), then out, image, templates
+    const size_t offQ = n * 8, offOut = 2 * n * 8, offImg = (offOut + nout * 4 + 255) / 256 * 256;
+    const size_t offT = (offImg + n + 255) / 256 * 256, total = offT + nt;
+    char *d = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&d), total, st);
+    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? NCC_ERR_NOMEM : NCC_ERR_CUDA;
+    int64_t *S = reinterpret_cast<int64_t *>(d), *Q = reinterpret_cast<int64_t *>(d + offQ);
+    float *dout = reinterpret_cast<float *>(d + offOut);
+    uint8_t *dimg = reinterpret_cast<uint8_t *>(d + offImg), *dt = reinterpret_cast<uint8_t *>(d + offT);
+    rc = NCC_OK;
+    if (cudaMemcpyAsync(dimg, img, n, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(dt, tmpl, nt, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        rc = NCC_ERR_CUDA;
+    if (rc == NCC_OK) rc = ncc_sat_build(dimg, W, H, S, Q, stream);
+    if (rc == NCC_OK) rc = ncc_correlate_bank(dimg, W, H, dt, wT, hT, nT, S, Q, dout, stream);
+    if (rc == NCC_OK &&
+        cudaMemcpyAsync(out, dout, nout * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        rc = NCC_ERR_CUDA;
+    cudaFreeAsync(d, st);
+    const int rs = ncc_sync_status(stream);
+    return rc != NCC_OK ? rc : rs;
+}
+
+int ncc_sync_status(ncc_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return NCC_ERR_CUDA;
+    int *status = nullptr;
+    int rc = status_ptr(&status);
+    if (rc != NCC_OK) return rc;
+    int v = 0;
+    if (cudaMemcpy(&v, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return NCC_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return NCC_ERR_CUDA;
+    }
+    return v;
+}
+
+const char *ncc_status_string(int status) {
+    switch (status) {
+        case NCC_OK: return "ok";
+        case NCC_ERR_INVALID_ARG: return "invalid argument";
+        case NCC_ERR_UNSUPPORTED: return "unsupported size or shape";
+        case NCC_ERR_CUDA: return "CUDA runtime error";
+        case NCC_ERR_TIMEOUT: return "look-back wait timed out";
+        case NCC_ERR_NOMEM: return "device workspace allocation failed";
+        default: return "unknown status";
+    }
+}
+
+int ncc_version(void) { return (0 << 16) | 1; }
+
+int ncc_debug_set_fault(int suppress_tile, uint64_t timeout_ns) {
+    if (suppress_tile < -1) return NCC_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_fault_tile = suppress_tile;
+    g_timeout_ns = timeout_ns ? timeout_ns : 1000000000ull;
+    return NCC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// ncc_common.cuh -- small device helpers and launch interfaces shared by the
+// library's translation units (inline PTX for the memory-model operations,
+// the bounded look-back wait, and the host launchers' declarations).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ncc.h"
+
+namespace ncc {
+
+// ---------------------------------------------------------------------------
+// Memory-model helpers (PTX ISA: ld.acquire / st.release at GPU scope).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Records the first error of a launch sequence in the per-device status word.
+__device__ __forceinline__ void record_status(int *status, int code) {
+    atomicCAS(status, 0, code);
+}
+
+// Look-back flag states (section 15.8's three-state protocol).
+enum : unsigned { FLAG_EMPTY = 0u, FLAG_AGGREGATE = 1u, FLAG_PREFIX = 2u };
+
+// Waits until *flag leaves FLAG_EMPTY and returns its state.  The wait is
+// bounded twice: by `timeout_ns` of %globaltimer since `t0`, and by an
+// iteration cap.  It also gives up when another CTA has raised *abort.  On
+// giving up it raises *abort, records NCC_ERR_TIMEOUT and returns
+// FLAG_EMPTY, so the caller can leave without publishing anything.
+__device__ __forceinline__ unsigned wait_flag(const unsigned *flag, unsigned *abort,
+                                              int *status, uint64_t t0,
+                                              uint64_t timeout_ns) {
+    unsigned f = ld_acquire_gpu(flag);
+    if (f != FLAG_EMPTY) return f;
+    unsigned backoff = 32;
+    for (unsigned it = 1;; ++it) {
+        __nanosleep(backoff);
+        if (backoff < 256) backoff <<= 1;
+        f = ld_acquire_gpu(flag);
+        if (f != FLAG_EMPTY) return f;
+        if ((it & 7u) == 0u) {
+            if (ld_relaxed_gpu(abort) != 0u) return FLAG_EMPTY;
+            if (global_timer_ns() - t0 > timeout_ns || it > (1u << 26)) {
+                atomicExch(abort, 1u);
+                record_status(status, NCC_ERR_TIMEOUT);
+                return FLAG_EMPTY;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers (defined in the kernel translation units).
+// ---------------------------------------------------------------------------
+
+// Summed-area tables: sizes of the look-back workspace for an image.
+struct SatPlan {
+    int tile_w, tile_h;     // tile shape in pixels
+    int ntx, nty;           // tiles per row / per column
+    size_t zero_bytes;      // leading bytes of the workspace that must be zero
+    size_t total_bytes;     // whole workspace
+};
+SatPlan sat_plan(int W, int H);
+cudaError_t sat_launch(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
+                       void *workspace, const SatPlan &plan, int *status,
+                       uint64_t timeout_ns, int fault_tile, cudaStream_t stream);
+
+// Single-template correlation (dp4a numerator + fused box-sum epilogue).
+struct CorrArgs {
+    const uint8_t *img;
+    int W, H;
+    const uint8_t *tmpl;
+    int wT, hT;
+    const int64_t *S, *Q;
+    float *out;                 // coefficients (null when moments are requested)
+    int64_t *sumI, *sumI2, *sumIT;  // moments (all null unless requested)
+    int *status;                // per-device status word
+};
+bool corr_dp4a_supported(int wT, int hT);
+cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream);
+
+// Template-bank correlation on the tensor cores (tcgen05, f16 operands,
+// fp32 accumulation; exact while wT*hT*255^2 < 2^24).
+struct BankArgs {
+    const uint8_t *img;
+    int W, H;
+    const uint8_t *tmpl;
+    int wT, hT, nT;
+    const int64_t *S, *Q;
+    float *out;
+    int64_t *sumI, *sumI2, *sumIT;
+    int *status;
+};
+bool bank_tc_supported(int W, int H, int wT, int hT, int nT);
+cudaError_t bank_tc_launch(const BankArgs &a, cudaStream_t stream);
+
+}  // namespace ncc

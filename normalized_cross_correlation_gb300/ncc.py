@@ -1,0 +1,218 @@
+"""Thin Python binding of the C ABI in include/ncc.h.
+
+Argument marshalling only: every step of the path runs in the CUDA kernels
+of libncc_gb300.so.  Tensors are torch tensors (PyTorch provides device
+memory and streams); the functions keep the C names.  There is no CPU
+fallback: if the library is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+from . import _build
+
+NCC_OK = 0
+NCC_ERR_INVALID_ARG = -1
+NCC_ERR_UNSUPPORTED = -2
+NCC_ERR_CUDA = -3
+NCC_ERR_TIMEOUT = -4
+NCC_ERR_NOMEM = -5
+
+EXPORTS = ("ncc_sat_build", "ncc_correlate", "ncc_correlate_bank", "ncc_correlate_moments",
+           "ncc_match_host", "ncc_sync_status", "ncc_status_string", "ncc_version",
+           "ncc_debug_set_fault")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class NccError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {code} ({status_text(code)})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library {path} is missing; build it with "
+                    "normalized_cross_correlation_gb300._build.build()")
+            L = ctypes.CDLL(path)
+            vp, i, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
+            L.ncc_sat_build.argtypes = [vp, i, i, vp, vp, vp]
+            L.ncc_correlate.argtypes = [vp, i, i, vp, i, i, vp, vp, vp, vp]
+            L.ncc_correlate_bank.argtypes = [vp, i, i, vp, i, i, i, vp, vp, vp, vp]
+            L.ncc_correlate_moments.argtypes = [vp, i, i, vp, i, i, i, vp, vp, vp, vp, vp, vp]
+            L.ncc_match_host.argtypes = [vp, i, i, vp, i, i, i, vp, vp]
+            L.ncc_sync_status.argtypes = [vp]
+            L.ncc_status_string.argtypes = [i]
+            L.ncc_status_string.restype = ctypes.c_char_p
+            L.ncc_version.argtypes = []
+            L.ncc_debug_set_fault.argtypes = [i, u64]
+            for name in EXPORTS:
+                if name != "ncc_status_string":
+                    getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def status_text(code: int) -> str:
+    try:
+        return lib().ncc_status_string(int(code)).decode()
+    except Exception:  # the text is only decoration for an error message
+        return "?"
+
+
+def _check(code: int, where: str) -> None:
+    if code != NCC_OK:
+        raise NccError(code, where)
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t, dtype, ndim: int, name: str):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype or t.dim() != ndim or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous {dtype} tensor with {ndim} dims")
+    return t
+
+
+def _tmpl3(t):
+    return t.unsqueeze(0) if t.dim() == 2 else t
+
+
+# --------------------------------------------------------------------------
+# Entry points (C names).
+# --------------------------------------------------------------------------
+
+def ncc_sat_build(img, S=None, Q=None, stream=None):
+    """S = SAT(I), Q = SAT(I^2): inclusive int64 tables of a uint8 [H][W] image."""
+    import torch
+    _dev(img, torch.uint8, 2, "img")
+    H, W = img.shape
+    if S is None:
+        S = torch.empty((H, W), dtype=torch.int64, device=img.device)
+    if Q is None:
+        Q = torch.empty((H, W), dtype=torch.int64, device=img.device)
+    _dev(S, torch.int64, 2, "S")
+    _dev(Q, torch.int64, 2, "Q")
+    _check(lib().ncc_sat_build(img.data_ptr(), W, H, S.data_ptr(), Q.data_ptr(),
+                               _stream_handle(stream)), "ncc_sat_build")
+    return S, Q
+
+
+def ncc_correlate(img, tmpl, S, Q, out=None, stream=None):
+    """fp32 [Oy][Ox] coefficients of one uint8 [hT][wT] template."""
+    import torch
+    _dev(img, torch.uint8, 2, "img")
+    _dev(tmpl, torch.uint8, 2, "tmpl")
+    H, W = img.shape
+    hT, wT = tmpl.shape
+    if out is None:
+        out = torch.empty((max(H - hT + 1, 0), max(W - wT + 1, 0)), dtype=torch.float32,
+                          device=img.device)
+    _dev(out, torch.float32, 2, "out")
+    _check(lib().ncc_correlate(img.data_ptr(), W, H, tmpl.data_ptr(), wT, hT, S.data_ptr(),
+                               Q.data_ptr(), out.data_ptr(), _stream_handle(stream)),
+           "ncc_correlate")
+    return out
+
+
+def ncc_correlate_bank(img, tmpls, S, Q, out=None, stream=None):
+    """fp32 [nT][Oy][Ox] coefficients of a uint8 [nT][hT][wT] template bank."""
+    import torch
+    _dev(img, torch.uint8, 2, "img")
+    tmpls = _tmpl3(tmpls)
+    _dev(tmpls, torch.uint8, 3, "tmpls")
+    H, W = img.shape
+    nT, hT, wT = tmpls.shape
+    if out is None:
+        out = torch.empty((nT, max(H - hT + 1, 0), max(W - wT + 1, 0)), dtype=torch.float32,
+                          device=img.device)
+    _dev(out, torch.float32, 3, "out")
+    _check(lib().ncc_correlate_bank(img.data_ptr(), W, H, tmpls.data_ptr(), wT, hT, nT,
+                                    S.data_ptr(), Q.data_ptr(), out.data_ptr(),
+                                    _stream_handle(stream)), "ncc_correlate_bank")
+    return out
+
+
+def ncc_correlate_moments(img, tmpls, S, Q, stream=None):
+    """(SumI [Oy][Ox], SumI2 [Oy][Ox], SumIT [nT][Oy][Ox]) as int64."""
+    import torch
+    _dev(img, torch.uint8, 2, "img")
+    tmpls = _tmpl3(tmpls)
+    _dev(tmpls, torch.uint8, 3, "tmpls")
+    H, W = img.shape
+    nT, hT, wT = tmpls.shape
+    Oy, Ox = max(H - hT + 1, 0), max(W - wT + 1, 0)
+    sI = torch.empty((Oy, Ox), dtype=torch.int64, device=img.device)
+    sI2 = torch.empty((Oy, Ox), dtype=torch.int64, device=img.device)
+    sIT = torch.empty((nT, Oy, Ox), dtype=torch.int64, device=img.device)
+    _check(lib().ncc_correlate_moments(img.data_ptr(), W, H, tmpls.data_ptr(), wT, hT, nT,
+                                       S.data_ptr(), Q.data_ptr(), sI.data_ptr(),
+                                       sI2.data_ptr(), sIT.data_ptr(), _stream_handle(stream)),
+           "ncc_correlate_moments")
+    return sI, sI2, sIT
+
+
+def ncc_match_host(img, tmpls, out=None, stream=None):
+    """The whole path on HOST buffers (numpy arrays or CPU tensors; pinned
+    tensors make the copies asynchronous).  Returns fp32 [nT][Oy][Ox] on the
+    host; synchronizes the stream."""
+    def host_ptr(a):
+        if isinstance(a, np.ndarray):
+            if not a.flags.c_contiguous:
+                raise TypeError("host arrays must be C-contiguous")
+            return a.ctypes.data, a.shape
+        if a.is_cuda or not a.is_contiguous():
+            raise TypeError("host tensors must be contiguous CPU tensors")
+        return a.data_ptr(), tuple(a.shape)
+
+    ip, ishape = host_ptr(img)
+    if len(tmpls.shape) == 2:
+        tmpls = tmpls.reshape((1,) + tuple(tmpls.shape))
+    tp, tshape = host_ptr(tmpls)
+    H, W = ishape
+    nT, hT, wT = tshape
+    if out is None:
+        out = np.empty((nT, H - hT + 1, W - wT + 1), np.float32)
+    op, _ = host_ptr(out)
+    _check(lib().ncc_match_host(ip, W, H, tp, wT, hT, nT, op, _stream_handle(stream)),
+           "ncc_match_host")
+    return out
+
+
+def ncc_sync_status(stream=None) -> int:
+    return int(lib().ncc_sync_status(_stream_handle(stream)))
+
+
+def ncc_status_string(code: int) -> str:
+    return lib().ncc_status_string(int(code)).decode()
+
+
+def ncc_version() -> int:
+    return int(lib().ncc_version())
+
+
+def ncc_debug_set_fault(suppress_tile: int, timeout_ns: int = 0) -> None:
+    _check(lib().ncc_debug_set_fault(int(suppress_tile), int(timeout_ns)), "ncc_debug_set_fault")

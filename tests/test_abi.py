@@ -1,0 +1,80 @@
+"""The C-ABI library builds, loads without a GPU and exports every entry
+point include/ncc.h declares; argument checks answer before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "ncc.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ncc_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("ncc_sat_build", "ncc_correlate", "ncc_correlate_bank", "ncc_sync_status",
+                 "ncc_status_string", "ncc_correlate_moments", "ncc_match_host"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(built_lib):
+    L = ctypes.CDLL(built_lib)
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in ncc.h but not exported"
+
+
+def test_binding_lists_every_declared_symbol():
+    from normalized_cross_correlation_gb300 import ncc
+    assert sorted(ncc.EXPORTS) == declared_functions()
+
+
+def test_status_strings_and_version(built_lib):
+    from normalized_cross_correlation_gb300 import ncc
+    assert ncc.ncc_status_string(0) == "ok"
+    assert "time" in ncc.ncc_status_string(ncc.NCC_ERR_TIMEOUT)
+    assert ncc.ncc_status_string(12345) == "unknown status"
+    assert ncc.ncc_version() >= 1
+
+
+def test_argument_checks_need_no_gpu(built_lib):
+    from normalized_cross_correlation_gb300 import ncc
+    L = ncc.lib()
+    fake = 4096  # never dereferenced: every call below fails its checks first
+    # null / non-positive sizes
+    assert L.ncc_sat_build(None, 16, 16, fake, fake * 4, None) == ncc.NCC_ERR_INVALID_ARG
+    assert L.ncc_sat_build(fake, 0, 16, fake * 4, fake * 8, None) == ncc.NCC_ERR_INVALID_ARG
+    assert L.ncc_sat_build(fake, 16, -1, fake * 4, fake * 8, None) == ncc.NCC_ERR_INVALID_ARG
+    # a row's running sum of squares must fit uint32: W <= 66051
+    assert L.ncc_sat_build(fake, 66052, 1, fake * 4, fake * 8, None) == ncc.NCC_ERR_UNSUPPORTED
+    # misaligned table pointers
+    assert L.ncc_sat_build(fake, 16, 16, fake * 4 + 4, fake * 8, None) == ncc.NCC_ERR_INVALID_ARG
+    # overlapping tables
+    assert L.ncc_sat_build(fake, 16, 16, fake * 4, fake * 4 + 8, None) == ncc.NCC_ERR_INVALID_ARG
+    # template larger than the image, empty bank
+    assert L.ncc_correlate(fake, 16, 16, fake, 17, 4, fake * 8, fake * 16, fake * 32,
+                           None) == ncc.NCC_ERR_INVALID_ARG
+    assert L.ncc_correlate_bank(fake, 16, 16, fake, 4, 4, 0, fake * 8, fake * 16, fake * 32,
+                                None) == ncc.NCC_ERR_INVALID_ARG
+    # SumIT must fit uint32: wT*hT <= 66051
+    assert L.ncc_correlate(fake, 300, 300, fake, 300, 300, fake * 1024, fake * 2048, fake * 4096,
+                           None) == ncc.NCC_ERR_UNSUPPORTED
+    # output overlapping an input
+    assert L.ncc_correlate(fake, 16, 16, fake * 2, 4, 4, fake * 8, fake * 16, fake * 8,
+                           None) == ncc.NCC_ERR_INVALID_ARG
+    assert L.ncc_match_host(None, 16, 16, fake, 4, 4, 1, fake, None) == ncc.NCC_ERR_INVALID_ARG
+    assert L.ncc_debug_set_fault(-2, 0) == ncc.NCC_ERR_INVALID_ARG
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "normalized_cross_correlation_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".c")):
+                text = open(os.path.join(dirpath, f), errors="ignore").read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "ncc_oracle" not in text, f
