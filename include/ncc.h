@@ -72,8 +72,12 @@ enum ncc_status_code {
  *   S, Q device, int64 [H][W], written completely; 8-byte aligned; must not
  *        overlap each other or img.
  * Single pass: a decoupled look-back scan over tiles, handed out in
- * row-major order so that every wait points at an earlier tile.  Uses a
- * stream-ordered workspace (cudaMallocAsync/cudaFreeAsync on `stream`).
+ * row-major order so that every wait points at an earlier tile.  The
+ * look-back state lives in a per-device workspace owned by the library: it
+ * is allocated (cudaMalloc) on the first call on a device and whenever a
+ * larger image needs more room -- make such a call before any stream
+ * capture -- and reused afterwards without clearing.  Calls on different
+ * streams are ordered through an event so they never share it concurrently.
  * Returns NCC_OK, NCC_ERR_INVALID_ARG, NCC_ERR_UNSUPPORTED, NCC_ERR_NOMEM or
  * NCC_ERR_CUDA.
  */

@@ -9,34 +9,39 @@
 // (SumI and SumI2 of every window from S and Q by the four-corner box sum).
 //
 // GB300 design:
-//   - Output tile: 128 shifts wide by 32 rows; 256 threads; each thread owns
-//     4 rows x 4 shifts.  Lane = 4*qg + d owns the shifts x0 + 16*qg + 4*k + d
-//     (k = 0..3).
+//   - Output tile: 128 shifts wide by 64 rows; 256 threads; each thread owns
+//     8 rows x 4 shifts.  Lane = 4*qg + d owns the shifts x0 + 16*qg + 4*k + d
+//     (k = 0..3) of rows 8*warp .. 8*warp+7.
 //   - The tile plus its (wT-1) x (hT-1) halo is one TMA box (cp.async.bulk.
 //     tensor, completion on an mbarrier).  Images whose rows are not a
-//     multiple of 16 bytes fall back to plain loads.
+//     multiple of 16 bytes, or boxes beyond the TMA limits, use plain loads.
 //   - Four byte-shifted copies of the staged tile (copy d starts d bytes
 //     later) let every lane read 32-bit-aligned groups of four pixels for its
 //     phase d, so the inner loop is two 16-byte shared loads per image row and
-//     template chunk plus 16 __dp4a per output row -- no byte permutes.  The
-//     copies sit 32 bytes (mod 128) apart so the eight lanes of each shared
-//     load phase hit distinct banks.
+//     template chunk plus, per output row, one broadcast 16-byte template load
+//     and 16 __dp4a -- no byte permutes.  The copies sit 32 bytes (mod 128)
+//     apart so the eight lanes of each shared-load phase hit distinct banks.
 //   - The template is packed into 32-bit words in shared memory, in chunks of
 //     16 pixels, zero-padded to a multiple of 16 (the zero bytes cancel any
 //     pixels read past the window).
 //   - SumIT accumulates in uint32 (exact while wT*hT*255^2 < 2^32).
+//   - Epilogue: the SumIT tile is transposed through shared memory so that
+//     lane L handles shifts x0 + 32*m + L; the eight corner loads per shift
+//     and the fp32 stores are then coalesced across the warp.  num and vI
+//     are exact int64; they are converted to fp32 through two 32-bit halves
+//     (the 64-bit convert runs on the slow fp64 pipe on this part).
 #include "ncc_common.cuh"
 
 #include <cuda.h>
-#include <math.h>
+#include <string.h>
 
 namespace ncc {
 namespace {
 
 constexpr int kOutW = 128;
-constexpr int kRowsPerThread = 4;
+constexpr int kRowsPerThread = 8;
 constexpr int kWarps = 8;
-constexpr int kOutH = kWarps * kRowsPerThread;
+constexpr int kOutH = kWarps * kRowsPerThread;  // 64
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxTmaBox = 256;        // TMA box extent limit per dimension
 constexpr int kMaxSmem = 227 * 1024;   // opt-in shared memory per CTA
@@ -57,7 +62,7 @@ Geom make_geom(int wT, int hT) {
     g.boxH = kOutH + hT - 1;
     const int copyBytes = g.boxW * g.boxH;
     g.copyStride = (copyBytes + 127) / 128 * 128 + 32;
-    g.tmplOff = 4 * g.copyStride;
+    g.tmplOff = 4 * g.copyStride;  // >= kOutH*kOutW*4: the SumIT transpose reuses the copies
     g.smemBytes = g.tmplOff + hT * g.nch * 16 + 128;
     return g;
 }
@@ -79,27 +84,28 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ long long box_sum(const long long *__restrict__ T, int W, int x, int y,
-                                             int w, int h) {
-    // four-corner rule over [x, x+w) x [y, y+h); row -1 / column -1 read as 0
-    const int xr = x + w - 1, yb = y + h - 1;
-    long long v = __ldg(&T[(size_t)yb * W + xr]);
-    if (y > 0) v -= __ldg(&T[(size_t)(y - 1) * W + xr]);
-    if (x > 0) v -= __ldg(&T[(size_t)yb * W + (x - 1)]);
-    if (x > 0 && y > 0) v += __ldg(&T[(size_t)(y - 1) * W + (x - 1)]);
-    return v;
+// fp32 value of a non-negative 64-bit integer below 2^56, rounded once:
+// hi * 2^32 + fl(lo) in one fma (the error of fl(lo) is below 2^-25 of the
+// total whenever hi > 0).
+__device__ __forceinline__ float u64_to_f32(unsigned long long a) {
+    return fmaf(__uint2float_rn((unsigned)(a >> 32)), 4294967296.0f,
+                __uint2float_rn((unsigned)a));
+}
+
+__device__ __forceinline__ float i64_to_f32(long long v) {
+    const float f = u64_to_f32(v < 0 ? (unsigned long long)(-v) : (unsigned long long)v);
+    return v < 0 ? -f : f;
 }
 
 template <bool kTma, bool kMoments>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const KParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     __shared__ __align__(8) unsigned long long s_bar;
-    __shared__ long long s_red[kWarps][2];
-    __shared__ long long s_sumT;
-    __shared__ long long s_vT;
+    __shared__ unsigned s_red[kWarps][2];
+    __shared__ long long s_sumT, s_vT;
     __shared__ float s_invSqrtVT;
 
     const Geom &g = p.g;
@@ -132,47 +138,46 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const KParams p) {
     // --- pack the template, template statistics (overlaps the TMA) -------
     uint32_t *tw = reinterpret_cast<uint32_t *>(smem + g.tmplOff);
     const int nWords = p.hT * g.nch * 4;
+    unsigned sa = 0, sb = 0;    // SumT < 2^25 and SumT2 < 2^32 (wT*hT <= 66051)
     for (int wi = tid; wi < nWords; wi += kThreads) {
         const int j = wi / (g.nch * 4), cw = wi - j * g.nch * 4;
         uint32_t v = 0;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             const int i = 4 * cw + b;
-            if (i < p.wT) v |= (uint32_t)__ldg(p.tmpl + (size_t)j * p.wT + i) << (8 * b);
+            if (i < p.wT) {
+                const unsigned t = __ldg(p.tmpl + (size_t)j * p.wT + i);
+                v |= t << (8 * b);
+                sa += t;
+                sb += t * t;
+            }
         }
         tw[wi] = v;
     }
-    {
-        long long a = 0, b = 0;
-        for (int i = tid; i < p.wT * p.hT; i += kThreads) {
-            const long long t = __ldg(p.tmpl + i);
-            a += t;
-            b += t * t;
-        }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            a += __shfl_xor_sync(0xffffffffu, a, o);
-            b += __shfl_xor_sync(0xffffffffu, b, o);
-        }
-        if (lane == 0) { s_red[warp][0] = a; s_red[warp][1] = b; }
+    for (int o = 16; o > 0; o >>= 1) {
+        sa += __shfl_xor_sync(0xffffffffu, sa, o);
+        sb += __shfl_xor_sync(0xffffffffu, sb, o);
     }
+    if (lane == 0) { s_red[warp][0] = sa; s_red[warp][1] = sb; }
     __syncthreads();
     if (tid == 0) {
-        long long a = 0, b = 0;
+        unsigned a = 0, b = 0;
         for (int w = 0; w < kWarps; ++w) { a += s_red[w][0]; b += s_red[w][1]; }
         const long long N = (long long)p.wT * p.hT;
+        const long long vT = N * (long long)b - (long long)a * (long long)a;
         s_sumT = a;
-        s_vT = N * b - a * a;
-        s_invSqrtVT = s_vT > 0 ? (float)(1.0 / sqrt((double)s_vT)) : 0.0f;
+        s_vT = vT;
+        s_invSqrtVT = vT > 0 ? __frsqrt_rn(u64_to_f32((unsigned long long)vT)) : 0.0f;
     }
     if (kTma) {
-        // every thread waits for the TMA transaction to land
+        // every thread waits for the TMA transaction to land (bounded)
         uint32_t done = 0;
         for (unsigned it = 0; !done; ++it) {
             asm volatile(
                 "{ .reg .pred P; mbarrier.try_wait.parity.shared::cta.b64 P, [%1], 0; selp.u32 %0, 1, 0, P; }"
                 : "=r"(done) : "r"(smem_u32(&s_bar)) : "memory");
-            if (it > (1u << 24)) {        // a TMA that never lands is reported, never a hang
+            if (it > (1u << 24)) {
                 record_status(p.status, NCC_ERR_TIMEOUT);
                 break;
             }
@@ -185,7 +190,8 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const KParams p) {
         const uint32_t *c0 = reinterpret_cast<const uint32_t *>(smem);
         const int words = (g.boxW * g.boxH) / 4;
         for (int wi = tid; wi < words; wi += kThreads) {
-            const uint32_t lo = c0[wi], hi = c0[wi + 1];  // c0[words] is padding: only meets zero template bytes
+            // c0[words] is padding: its bytes only meet zero template bytes
+            const uint32_t lo = c0[wi], hi = c0[wi + 1];
             reinterpret_cast<uint32_t *>(smem + 1 * g.copyStride)[wi] = __byte_perm(lo, hi, 0x4321);
             reinterpret_cast<uint32_t *>(smem + 2 * g.copyStride)[wi] = __byte_perm(lo, hi, 0x5432);
             reinterpret_cast<uint32_t *>(smem + 3 * g.copyStride)[wi] = __byte_perm(lo, hi, 0x6543);
@@ -193,7 +199,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const KParams p) {
     }
     __syncthreads();
 
-    // --- numerator: SumIT for 4 rows x 4 shifts per thread -----------------
+    // --- numerator: SumIT for 8 rows x 4 shifts per thread -----------------
     const int qg = lane >> 2, d = lane & 3;
     const uint8_t *cp = smem + d * g.copyStride + 16 * qg;
     uint32_t acc[kRowsPerThread][4];
@@ -230,31 +236,49 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const KParams p) {
         }
     }
 
+    // --- transpose SumIT through shared memory ------------------------------
+    __syncthreads();  // every warp is done with the staged copies
+    uint32_t *sIT = reinterpret_cast<uint32_t *>(smem) + warp * kRowsPerThread * kOutW;
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sIT[i * kOutW + 16 * qg + 4 * k + d] = acc[i][k];
+    __syncwarp();
+
     // --- epilogue: moments from S and Q, coefficient -----------------------
     const long long N = (long long)p.wT * p.hT;
     const long long sT = s_sumT, vT = s_vT;
     const float invSqrtVT = s_invSqrtVT;
-#pragma unroll
+    const size_t W = (size_t)p.W;
     for (int i = 0; i < kRowsPerThread; ++i) {
         const int y = y0 + warp * kRowsPerThread + i;
         if (y >= p.Oy) break;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int x = x0 + 16 * qg + 4 * k + d;
-            if (x >= p.Ox) continue;
-            const long long sI = box_sum(p.S, p.W, x, y, p.wT, p.hT);
-            const long long sI2 = box_sum(p.Q, p.W, x, y, p.wT, p.hT);
+        const long long *St = p.S + (size_t)(y - 1) * W, *Sb = p.S + (size_t)(y + p.hT - 1) * W;
+        const long long *Qt = p.Q + (size_t)(y - 1) * W, *Qb = p.Q + (size_t)(y + p.hT - 1) * W;
+#pragma unroll 2
+        for (int m = 0; m < 4; ++m) {
+            const int xo = 32 * m + lane, x = x0 + xo;
+            if (x >= p.Ox) break;
+            const int xl = x - 1, xr = x + p.wT - 1;
+            long long sI = __ldg(Sb + xr), sI2 = __ldg(Qb + xr);
+            if (y > 0) { sI -= __ldg(St + xr); sI2 -= __ldg(Qt + xr); }
+            if (x > 0) { sI -= __ldg(Sb + xl); sI2 -= __ldg(Qb + xl); }
+            if (x > 0 && y > 0) { sI += __ldg(St + xl); sI2 += __ldg(Qt + xl); }
+            const unsigned sumIT = sIT[i * kOutW + xo];
             const size_t o = (size_t)y * p.Ox + x;
             if (kMoments) {
                 p.sumI[o] = sI;
                 p.sumI2[o] = sI2;
-                p.sumIT[o] = (long long)acc[i][k];
+                p.sumIT[o] = (long long)sumIT;
             } else {
-                const long long num = N * (long long)acc[i][k] - sI * sT;
-                const long long vI = N * sI2 - sI * sI;
+                // |SumI| < 2^25 and SumT < 2^25; SumI2 < 2^32
+                const long long num = (long long)((unsigned long long)N * sumIT) -
+                                      (long long)((int)sI) * (long long)((int)sT);
+                const long long vI = (long long)((unsigned long long)N * (unsigned)sI2) -
+                                     (long long)((int)sI) * (long long)((int)sI);
                 float r = 0.0f;
                 if (vI > 0 && vT > 0) {
-                    r = (float)num * rsqrtf((float)vI) * invSqrtVT;
+                    r = i64_to_f32(num) * rsqrtf(u64_to_f32((unsigned long long)vI)) * invSqrtVT;
                     r = fminf(1.0f, fmaxf(-1.0f, r));
                 }
                 __stcs(p.out + o, r);

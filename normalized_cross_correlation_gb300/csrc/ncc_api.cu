@@ -112,25 +112,15 @@ int ncc_sat_build(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
     int *status = nullptr;
     rc = status_ptr(&status);
     if (rc != NCC_OK) return rc;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const ncc::SatPlan plan = ncc::sat_plan(W, H);
-    void *ws = nullptr;
-    cudaError_t e = cudaMallocAsync(&ws, plan.total_bytes, st);
-    if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? NCC_ERR_NOMEM : NCC_ERR_CUDA;
-    e = cudaMemsetAsync(ws, 0, plan.zero_bytes, st);
-    if (e == cudaSuccess) {
-        int fault;
-        uint64_t timeout;
-        {
-            std::lock_guard<std::mutex> lock(g_mutex);
-            fault = g_fault_tile;
-            timeout = g_timeout_ns;
-        }
-        e = ncc::sat_launch(img, W, H, S, Q, ws, plan, status, timeout, fault, st);
+    int fault;
+    uint64_t timeout;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        fault = g_fault_tile;
+        timeout = g_timeout_ns;
     }
-    cudaError_t ef = cudaFreeAsync(ws, st);
-    if (e != cudaSuccess) return to_status(e);
-    return to_status(ef);
+    return to_status(ncc::sat_build_run(img, W, H, S, Q, status, timeout, fault,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int ncc_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT,

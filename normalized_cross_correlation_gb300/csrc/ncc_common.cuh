@@ -74,17 +74,25 @@ __device__ __forceinline__ unsigned wait_flag(const unsigned *flag, unsigned *ab
 // Host launchers (defined in the kernel translation units).
 // ---------------------------------------------------------------------------
 
-// Summed-area tables: sizes of the look-back workspace for an image.
+// Summed-area tables: tiling and look-back workspace size for an image.
 struct SatPlan {
     int tile_w, tile_h;     // tile shape in pixels
     int ntx, nty;           // tiles per row / per column
-    size_t zero_bytes;      // leading bytes of the workspace that must be zero
+    size_t zero_bytes;      // leading bytes of the workspace that must start at zero
     size_t total_bytes;     // whole workspace
 };
 SatPlan sat_plan(int W, int H);
+// One launch of the builder on a caller-provided workspace.  `epoch` (1..31)
+// tags this call's look-back words; `ticket_base` is the workspace's ticket
+// counter value before the launch (it advances by ntx*nty per launch).
 cudaError_t sat_launch(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
-                       void *workspace, const SatPlan &plan, int *status,
-                       uint64_t timeout_ns, int fault_tile, cudaStream_t stream);
+                       void *workspace, const SatPlan &plan, uint32_t epoch,
+                       unsigned long long ticket_base, int *status, uint64_t timeout_ns,
+                       int fault_tile, cudaStream_t stream);
+// The builder on the library's per-device workspace (allocated on first use).
+cudaError_t sat_build_run(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
+                          int *status, uint64_t timeout_ns, int fault_tile,
+                          cudaStream_t stream);
 
 // Single-template correlation (dp4a numerator + fused box-sum epilogue).
 struct CorrArgs {

@@ -63,7 +63,8 @@ def test_coefficients_match_oracle(ncc, threads, W, H, wT, hT):
     assert r.shape == ref.shape
     np.testing.assert_allclose(r, ref, rtol=0, atol=TOL)
     _, x, y = w.crops[0]
-    assert abs(r[y, x] - 1.0) <= TOL
+    if wT * hT > 1:                                  # a 1-pixel template has zero variance
+        assert abs(r[y, x] - 1.0) <= TOL
     assert np.all(np.abs(r) <= 1.0)
 
 
