@@ -85,6 +85,29 @@ int ncc_sat_build(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
                   ncc_stream_t stream);
 
 /*
+ * ncc_sat_build_noalloc -- ncc_sat_build for callers that cannot allocate
+ * device memory (the pages have no counterpart: it is an interface
+ * addition).  Callers inside a CUDA stream capture, a host callback, a
+ * real-time loop, or a framework that owns every device allocation through
+ * its own pool cannot let a library call cudaMalloc/cudaFree (not
+ * capturable; may synchronize the device; bypasses their budget).  This
+ * entry point allocates nothing: its look-back scratch is a fixed 8 MiB
+ * array compiled into the library, which every GPU that loads the library
+ * holds until the process exits.
+ *   Arguments, layouts, results and errors as ncc_sat_build, plus:
+ *   NCC_ERR_UNSUPPORTED when the image needs more scratch than 8 MiB, i.e.
+ *   when ceil(W/128) * ceil(H/64) > 3276 tiles (4096x4096 fits; 8192x8192
+ *   does not).
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress); make it before any stream capture.  All calls on
+ * a device share the array and each clears what it needs to start at zero;
+ * calls whose kernels overlap on the GPU race on it, so order them (one
+ * stream, or events).
+ */
+int ncc_sat_build_noalloc(const uint8_t *img, int W, int H, int64_t *S,
+                          int64_t *Q, ncc_stream_t stream);
+
+/*
  * ncc_correlate -- one template, every valid shift (Listing 15-5's sums,
  * section 15.8's box sums, the coefficient above).
  *   img  device uint8 [H][W].

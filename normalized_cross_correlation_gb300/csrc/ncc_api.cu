@@ -99,6 +99,12 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
 
 }  // namespace
 
+namespace ncc {
+// The per-device status word's device address, for entry points defined in
+// other translation units.
+int status_word(int **out) { return status_ptr(out); }
+}  // namespace ncc
+
 extern "C" {
 
 int ncc_sat_build(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,

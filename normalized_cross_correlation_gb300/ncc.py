@@ -22,7 +22,7 @@ NCC_ERR_CUDA = -3
 NCC_ERR_TIMEOUT = -4
 NCC_ERR_NOMEM = -5
 
-EXPORTS = ("ncc_sat_build", "ncc_correlate", "ncc_correlate_bank", "ncc_correlate_moments",
+EXPORTS = ("ncc_sat_build", "ncc_sat_build_noalloc", "ncc_correlate", "ncc_correlate_bank", "ncc_correlate_moments",
            "ncc_match_host", "ncc_sync_status", "ncc_status_string", "ncc_version",
            "ncc_debug_set_fault")
 
@@ -53,6 +53,7 @@ def lib() -> ctypes.CDLL:
             L = ctypes.CDLL(path)
             vp, i, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
             L.ncc_sat_build.argtypes = [vp, i, i, vp, vp, vp]
+            L.ncc_sat_build_noalloc.argtypes = [vp, i, i, vp, vp, vp]
             L.ncc_correlate.argtypes = [vp, i, i, vp, i, i, vp, vp, vp, vp]
             L.ncc_correlate_bank.argtypes = [vp, i, i, vp, i, i, i, vp, vp, vp, vp]
             L.ncc_correlate_moments.argtypes = [vp, i, i, vp, i, i, i, vp, vp, vp, vp, vp, vp]
@@ -118,6 +119,19 @@ def ncc_sat_build(img, S=None, Q=None, stream=None):
     _dev(Q, torch.int64, 2, "Q")
     _check(lib().ncc_sat_build(img.data_ptr(), W, H, S.data_ptr(), Q.data_ptr(),
                                _stream_handle(stream)), "ncc_sat_build")
+    return S, Q
+
+
+def ncc_sat_build_noalloc(img, S, Q, stream=None):
+    """ncc_sat_build without any device allocation, into caller tables S, Q
+    (int64 [H][W]); for callers that cannot allocate (see include/ncc.h)."""
+    import torch
+    _dev(img, torch.uint8, 2, "img")
+    _dev(S, torch.int64, 2, "S")
+    _dev(Q, torch.int64, 2, "Q")
+    H, W = img.shape
+    _check(lib().ncc_sat_build_noalloc(img.data_ptr(), W, H, S.data_ptr(), Q.data_ptr(),
+                                       _stream_handle(stream)), "ncc_sat_build_noalloc")
     return S, Q
 
 
