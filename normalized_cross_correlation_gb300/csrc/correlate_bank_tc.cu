@@ -1,12 +1,459 @@
-// correlate_bank_tc.cu -- template-bank correlation on the tensor cores
-// (placeholder until the tcgen05 kernel lands: banks run template by
-// template on the dp4a kernel).
+// correlate_bank_tc.cu -- a bank of nT templates against every valid shift of
+// an 8-bit image, with the numerator on the 5th-generation tensor cores
+// (tcgen05.mma kind::f16, fp32 accumulation in tensor memory) and a fused
+// epilogue that reads the window moments from the summed-area tables once
+// per shift and writes the fp32 coefficients of every template.
+//
+// Follows The CUDA Handbook, chapter 15: section 15.8 (one SAT pair serves
+// every template of a bank; the four-corner box sum) and "Image in shared
+// memory", Listing 15-5 (the per-shift SumIT).  For a bank the numerator is
+// a dense contraction: for output row y and the 128 shifts x0..x0+127,
+//     D[m][n] = sum_j sum_i I[y+j][x0+m+i] * T_n[j][i],
+// i.e. for each template row j one MMA with M = 128 shifts, N = templates,
+// K = 16 template columns (more K chunks for wider templates).
+//
+// Operands (no im2col): the A operand of image row r is MN-major with both
+// core-matrix strides 128 bytes over a buffer holding eight copies of the
+// row segment shifted by 0..7 pixels (block b, copy s, element e = pixel
+// 8b+s+e), so element (m, k) sits at pixel m+k: one 2.2 KB buffer per image
+// row serves all hT output rows that use it.  B is K-major, template row j,
+// all templates.  Pixels 0..255 are exact in f16 and every product and
+// partial sum is an integer below 2^24, so the fp32 accumulation is exact
+// while a template group has at most 258 pixels; taller templates are
+// split into row groups with separate accumulators, summed as integers.
+//
+// Warp roles (persistent CTAs, 2 per SM):
+//   warp 0     allocates tensor memory; one thread issues the MMAs and the
+//              commits (tcgen05.commit -> mbarrier),
+//   warps 1-3  convert image rows (u8 -> f16 shifted copies) into a ring of
+//              A buffers in shared memory,
+//   warps 4-7  epilogue: tcgen05.ld one accumulator row per thread (thread
+//              = shift), box sums from S and Q once per shift, exact int64
+//              num and vI, fp32 coefficient per template, coalesced stores.
+// All hand-offs are mbarriers; every wait is bounded and a wait that runs out
+// records NCC_ERR_TIMEOUT and lets the CTA finish (never a hang).
 #include "ncc_common.cuh"
 
+#include <cuda_fp16.h>
+
 namespace ncc {
+namespace {
 
-bool bank_tc_supported(int, int, int, int, int) { return false; }
+constexpr int kThreads = 256;
+constexpr int kM = 128;               // shifts per tile (MMA M)
+constexpr int kTY = 32;               // output rows per tile
+constexpr int kProducers = 96;        // warps 1-3
+constexpr int kEpi0 = 128;            // first epilogue thread (warps 4-7)
+constexpr int kMaxExactPixels = 258;  // 258 * 255^2 < 2^24: exact fp32 accumulation
+constexpr int kMaxSmem = 110 * 1024;  // two CTAs per SM
+constexpr int kMaxTmemCols = 256;     // per CTA (two CTAs share 512 columns)
 
-cudaError_t bank_tc_launch(const BankArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+struct BankGeom {
+    int nTpad;      // templates padded to a multiple of 16 (MMA N)
+    int nK16;       // 16-column template chunks (MMA K steps per template row)
+    int G;          // template rows per exact accumulator group
+    int nG;         // groups
+    int accCols;    // tensor-memory columns per accumulator (nTpad * nG)
+    int na;         // accumulator stages
+    int tmemCols;   // allocated columns (power of two >= na * accCols)
+    int xBlocks;    // 8-pixel blocks per A buffer
+    int xBytes;     // bytes per A buffer
+    int nx;         // A buffers in the ring
+    int bBytes;     // B operand bytes (all template rows and chunks)
+    int offB, offX, offSt, offBar, smemBytes;
+};
+
+int pow2_at_least(int v) {
+    int p = 32;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+bool make_geom(int wT, int hT, int nT, BankGeom &g) {
+    if (wT > kMaxExactPixels) return false;
+    g.nTpad = (nT + 15) / 16 * 16;
+    if (g.nTpad > 256) return false;
+    g.nK16 = (wT + 15) / 16;
+    g.G = kMaxExactPixels / wT;
+    if (g.G > hT) g.G = hT;
+    g.nG = (hT + g.G - 1) / g.G;
+    g.accCols = g.nTpad * g.nG;
+    if (g.accCols > kMaxTmemCols) return false;
+    g.na = kMaxTmemCols / g.accCols;
+    if (g.na > 4) g.na = 4;
+    g.tmemCols = pow2_at_least(g.na * g.accCols);
+    if (g.tmemCols > kMaxTmemCols) return false;
+    g.xBlocks = 15 + 2 * g.nK16;
+    g.xBytes = g.xBlocks * 128;
+    g.nx = hT + 4;
+    g.bBytes = hT * g.nK16 * g.nTpad * 32;
+    g.offB = 0;
+    g.offX = (g.bBytes + 1023) / 1024 * 1024;
+    g.offSt = g.offX + g.nx * g.xBytes;
+    const int stBytes = g.nTpad * (8 + 8 + 4);
+    g.offBar = (g.offSt + stBytes + 15) / 16 * 16;
+    const int barBytes = (2 * g.nx + 2 * g.na) * 8 + 16;
+    g.smemBytes = g.offBar + barBytes + 1024;  // + alignment slack
+    return g.smemBytes <= kMaxSmem;
+}
+
+struct BParams {
+    const uint8_t *img;
+    int W, H;
+    const uint8_t *tmpl;
+    int wT, hT, nT;
+    const long long *S, *Q;
+    float *out;
+    long long *sumI, *sumI2, *sumIT;
+    int *status;
+    int Ox, Oy, ntx, ntiles;
+    BankGeom g;
+};
+
+__device__ __forceinline__ uint32_t saddr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ float u64_to_f32(unsigned long long a) {
+    return fmaf(__uint2float_rn((unsigned)(a >> 32)), 4294967296.0f, __uint2float_rn((unsigned)a));
+}
+
+__device__ __forceinline__ float i64_to_f32(long long v) {
+    const float f = u64_to_f32(v < 0 ? (unsigned long long)(-v) : (unsigned long long)v);
+    return v < 0 ? -f : f;
+}
+
+// shared-memory matrix descriptor, no swizzle (tcgen05 version field = 1)
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)(lbo >> 4) << 16) |
+           ((uint64_t)(sbo >> 4) << 32) | (1ull << 46);
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long *b, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(unsigned long long *b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+
+// Bounded wait for the phase with the given parity.  After the first wait
+// that runs out, *abort short-circuits every later wait of the CTA.
+__device__ __forceinline__ void mbar_wait(unsigned long long *b, uint32_t parity, int *abort,
+                                          int *status) {
+    if (*(volatile int *)abort) return;
+    uint32_t done = 0;
+    const uint64_t t0 = global_timer_ns();
+    for (unsigned it = 0; !done; ++it) {
+        asm volatile(
+            "{ .reg .pred P; mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2; selp.u32 %0, 1, 0, P; }"
+            : "=r"(done) : "r"(saddr(b)), "r"(parity) : "memory");
+        if (!done && (it & 1023u) == 1023u) {
+            if (*(volatile int *)abort) return;
+            if (global_timer_ns() - t0 > 2000000000ull || it > (1u << 26)) {
+                *(volatile int *)abort = 1;
+                record_status(status, NCC_ERR_TIMEOUT);
+                return;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tc_commit(unsigned long long *b) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(saddr(b)) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+}
+
+// Two pixels (bytes lo, hi of `w` selected by `sel`) as exact f16x2: the
+// byte is placed in the mantissa of 1024.0h and 1024 is subtracted.
+__device__ __forceinline__ uint32_t bytes_to_h2(uint32_t w, uint32_t sel) {
+    const uint32_t biased = __byte_perm(w, 0x64646464u, sel);
+    __half2 h = *reinterpret_cast<const __half2 *>(&biased);
+    h = __hsub2(h, __halves2half2(__float2half(1024.f), __float2half(1024.f)));
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <bool kMoments>
+__global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    const BankGeom &g = p.g;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    int *sT = reinterpret_cast<int *>(smem + g.offSt);                        // [nTpad]
+    long long *vT = reinterpret_cast<long long *>(smem + g.offSt + 4 * g.nTpad);  // [nTpad]
+    float *invs = reinterpret_cast<float *>(smem + g.offSt + 12 * g.nTpad);   // [nTpad]
+    unsigned long long *bar = reinterpret_cast<unsigned long long *>(smem + g.offBar);
+    unsigned long long *xfull = bar, *xempty = bar + g.nx;
+    unsigned long long *afull = bar + 2 * g.nx, *aempty = afull + g.na;
+
+    // --- prologue: B operand, template statistics, barriers, tensor memory ---
+    {
+        const int perRow = g.nK16 * g.nTpad * 16;  // f16 elements per template row
+        const int total = p.hT * perRow;
+        for (int e = tid; e < total; e += kThreads) {
+            const int j = e / perRow, rem = e - j * perRow;
+            const int c = rem / (g.nTpad * 16), r2 = rem - c * g.nTpad * 16;
+            const int n = r2 >> 4, k = r2 & 15;
+            const int col = 16 * c + k;
+            const float v = (n < p.nT && col < p.wT)
+                                ? (float)__ldg(p.tmpl + ((size_t)n * p.hT + j) * p.wT + col) : 0.f;
+            // K-major core matrices: (k/8) * nTpad*16 + (n/8) * 128 + (n%8) * 16 + (k%8) * 2
+            const int off = (j * g.nK16 + c) * g.nTpad * 32 + (k >> 3) * g.nTpad * 16 +
+                            (n >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2;
+            *reinterpret_cast<__half *>(smem + g.offB + off) = __float2half(v);
+        }
+        const long long N = (long long)p.wT * p.hT;
+        for (int n = tid; n < g.nTpad; n += kThreads) {
+            unsigned a = 0, b = 0;
+            if (n < p.nT) {
+                const uint8_t *t = p.tmpl + (size_t)n * p.wT * p.hT;
+                for (int i = 0; i < p.wT * p.hT; ++i) {
+                    const unsigned v = __ldg(t + i);
+                    a += v;
+                    b += v * v;
+                }
+            }
+            const long long v2 = N * (long long)b - (long long)a * (long long)a;
+            sT[n] = (int)a;
+            vT[n] = v2;
+            invs[n] = (n < p.nT && v2 > 0) ? __frsqrt_rn(u64_to_f32((unsigned long long)v2)) : 0.f;
+        }
+        if (tid == 0) {
+            for (int i = 0; i < g.nx; ++i) { mbar_init(&xfull[i], kProducers); mbar_init(&xempty[i], 1); }
+            for (int i = 0; i < g.na; ++i) { mbar_init(&afull[i], 1); mbar_init(&aempty[i], kThreads - kEpi0); }
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            s_abort = 0;
+        }
+        if (warp == 0) {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                         ::"r"(saddr(&s_tmem)), "r"(g.tmemCols) : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    }
+    const uint32_t tmem = s_tmem;
+    const long long N = (long long)p.wT * p.hT;
+    // instruction descriptor: D f32, A/B f16, A MN-major, B K-major, N, M = 128
+    const uint32_t idesc = (1u << 4) | (1u << 15) | ((uint32_t)(g.nTpad >> 3) << 17) |
+                           ((uint32_t)(kM >> 4) << 24);
+
+    uint32_t rowSeq = 0, outSeq = 0;  // image rows / output rows handled so far (all tiles)
+    for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
+        const int xt = tile % p.ntx, yb = tile / p.ntx;
+        const int x0 = xt * kM, y0 = yb * kTY;
+        const int ty = min(kTY, p.Oy - y0);
+        const int nrows = ty + p.hT - 1;
+
+        if (warp >= 1 && warp <= 3) {
+            // ---- producers: image rows -> f16 shifted-copy A buffers ----
+            const int pt = tid - 32;
+            for (int rl = 0; rl < nrows; ++rl) {
+                const uint32_t q = rowSeq + rl, slot = q % g.nx, k = q / g.nx;
+                if (k > 0) mbar_wait(&xempty[slot], (k - 1) & 1, &s_abort, p.status);
+                uint8_t *X = smem + g.offX + slot * g.xBytes;
+                const uint8_t *src = p.img + (size_t)(y0 + rl) * p.W;
+                for (int row = pt; row < g.xBlocks * 8; row += kProducers) {
+                    const int c0 = x0 + 8 * (row >> 3) + (row & 7);  // pixel of element 0
+                    uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (c0 + e < p.W) w0 |= (uint32_t)__ldg(src + c0 + e) << (8 * e);
+                        if (c0 + 4 + e < p.W) w1 |= (uint32_t)__ldg(src + c0 + 4 + e) << (8 * e);
+                    }
+                    uint4 h;
+                    h.x = bytes_to_h2(w0, 0x4140);
+                    h.y = bytes_to_h2(w0, 0x4342);
+                    h.z = bytes_to_h2(w1, 0x4140);
+                    h.w = bytes_to_h2(w1, 0x4342);
+                    *reinterpret_cast<uint4 *>(X + row * 16) = h;
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(&xfull[slot]);
+            }
+        } else if (warp == 0) {
+            // ---- MMA issuer ----
+            if (lane == 0) {
+                int ready = 0;  // image rows of this tile known to be converted
+                for (int yl = 0; yl < ty; ++yl) {
+                    const uint32_t o = outSeq + yl, a = o % g.na, ka = o / g.na;
+                    if (ka > 0) mbar_wait(&aempty[a], (ka - 1) & 1, &s_abort, p.status);
+                    while (ready < yl + p.hT) {
+                        const uint32_t q = rowSeq + ready;
+                        mbar_wait(&xfull[q % g.nx], (q / g.nx) & 1, &s_abort, p.status);
+                        ++ready;
+                    }
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t d = tmem + a * g.accCols;
+                    for (int j = 0; j < p.hT; ++j) {
+                        const uint32_t q = rowSeq + yl + j;
+                        const uint32_t xa = saddr(smem + g.offX + (q % g.nx) * g.xBytes);
+                        const uint32_t ba = saddr(smem + g.offB + j * g.nK16 * g.nTpad * 32);
+                        const int grp = j / g.G;
+                        for (int c = 0; c < g.nK16; ++c) {
+                            const uint64_t ad = smem_desc(xa + 256 * c, 128, 128);
+                            const uint64_t bd = smem_desc(ba + c * g.nTpad * 32, g.nTpad * 16, 128);
+                            tc_mma(d + grp * g.nTpad, ad, bd, idesc, (j % g.G != 0 || c != 0) ? 1u : 0u);
+                        }
+                    }
+                    tc_commit(&afull[a]);
+                    tc_commit(&xempty[(rowSeq + yl) % g.nx]);  // image row y0+yl is done
+                }
+                for (int rl = ty; rl < nrows; ++rl) tc_commit(&xempty[(rowSeq + rl) % g.nx]);
+            }
+            __syncwarp();
+        } else {
+            // ---- epilogue: thread = shift x0 + et ----
+            const int et = tid - kEpi0;
+            const int x = x0 + et;
+            const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+            const bool xin = x < p.Ox;
+            for (int yl = 0; yl < ty; ++yl) {
+                const int y = y0 + yl;
+                const uint32_t o = outSeq + yl, a = o % g.na, ka = o / g.na;
+                long long sI = 0, sI2 = 0;
+                if (xin) {
+                    const size_t W = (size_t)p.W;
+                    const int xl = x - 1, xr = x + p.wT - 1, yt = y - 1, ybm = y + p.hT - 1;
+                    sI = __ldg(p.S + (size_t)ybm * W + xr);
+                    sI2 = __ldg(p.Q + (size_t)ybm * W + xr);
+                    if (yt >= 0) { sI -= __ldg(p.S + (size_t)yt * W + xr); sI2 -= __ldg(p.Q + (size_t)yt * W + xr); }
+                    if (xl >= 0) { sI -= __ldg(p.S + (size_t)ybm * W + xl); sI2 -= __ldg(p.Q + (size_t)ybm * W + xl); }
+                    if (xl >= 0 && yt >= 0) { sI += __ldg(p.S + (size_t)yt * W + xl); sI2 += __ldg(p.Q + (size_t)yt * W + xl); }
+                }
+                const long long vI = (long long)((unsigned long long)N * (unsigned)sI2) -
+                                     (long long)((int)sI) * (long long)((int)sI);
+                const float rsI = vI > 0 ? rsqrtf(u64_to_f32((unsigned long long)vI)) : 0.f;
+                mbar_wait(&afull[a], ka & 1, &s_abort, p.status);
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (kMoments && xin) {
+                    const size_t o1 = (size_t)y * p.Ox + x;
+                    p.sumI[o1] = sI;
+                    p.sumI2[o1] = sI2;
+                }
+                for (int cc = 0; cc < g.nTpad; cc += 32) {
+                    uint32_t sum[32];
+                    {
+                        uint32_t v[32];
+                        tc_ld32(tmem + lane_base + a * g.accCols + cc, v);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) sum[i] = __float2uint_rn(__uint_as_float(v[i]));
+                    }
+                    for (int gi = 1; gi < g.nG; ++gi) {
+                        uint32_t v[32];
+                        tc_ld32(tmem + lane_base + a * g.accCols + gi * g.nTpad + cc, v);
+                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) sum[i] += __float2uint_rn(__uint_as_float(v[i]));
+                    }
+                    if (xin) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int t = cc + i;
+                            if (t >= p.nT) continue;
+                            const size_t oo = ((size_t)t * p.Oy + y) * p.Ox + x;
+                            if (kMoments) {
+                                p.sumIT[oo] = (long long)sum[i];
+                            } else {
+                                const long long num = (long long)((unsigned long long)N * sum[i]) -
+                                                      (long long)((int)sI) * (long long)sT[t];
+                                float r = i64_to_f32(num) * rsI * invs[t];
+                                r = fminf(1.0f, fmaxf(-1.0f, r));
+                                __stcs(p.out + oo, r);
+                            }
+                        }
+                    }
+                }
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                mbar_arrive(&aempty[a]);
+            }
+        }
+        rowSeq += nrows;
+        outSeq += ty;
+    }
+
+    // --- teardown: every accumulator has been drained by the epilogue ---
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     ::"r"(tmem), "r"(g.tmemCols) : "memory");
+}
+
+int g_num_sms[64] = {};
+
+}  // namespace
+
+bool bank_tc_supported(int W, int H, int wT, int hT, int nT) {
+    (void)W;
+    (void)H;
+    BankGeom g;
+    return nT >= 2 && make_geom(wT, hT, nT, g);
+}
+
+cudaError_t bank_tc_launch(const BankArgs &a, cudaStream_t stream) {
+    BParams p;
+    p.img = a.img; p.W = a.W; p.H = a.H;
+    p.tmpl = a.tmpl; p.wT = a.wT; p.hT = a.hT; p.nT = a.nT;
+    p.S = reinterpret_cast<const long long *>(a.S);
+    p.Q = reinterpret_cast<const long long *>(a.Q);
+    p.out = a.out;
+    p.sumI = reinterpret_cast<long long *>(a.sumI);
+    p.sumI2 = reinterpret_cast<long long *>(a.sumI2);
+    p.sumIT = reinterpret_cast<long long *>(a.sumIT);
+    p.status = a.status;
+    p.Ox = a.W - a.wT + 1;
+    p.Oy = a.H - a.hT + 1;
+    p.ntx = (p.Ox + kM - 1) / kM;
+    p.ntiles = p.ntx * ((p.Oy + kTY - 1) / kTY);
+    if (!make_geom(a.wT, a.hT, a.nT, p.g)) return cudaErrorNotSupported;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!g_num_sms[dev]) {
+        e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const int grid = p.ntiles < 2 * g_num_sms[dev] ? p.ntiles : 2 * g_num_sms[dev];
+    const size_t smem = (size_t)p.g.smemBytes;
+    if (a.sumIT) {
+        e = cudaFuncSetAttribute(bank_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        bank_tc_kernel<true><<<grid, kThreads, smem, stream>>>(p);
+    } else {
+        e = cudaFuncSetAttribute(bank_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        bank_tc_kernel<false><<<grid, kThreads, smem, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
 
 }  // namespace ncc

@@ -25,11 +25,18 @@
 //     16 pixels, zero-padded to a multiple of 16 (the zero bytes cancel any
 //     pixels read past the window).
 //   - SumIT accumulates in uint32 (exact while wT*hT*255^2 < 2^32).
-//   - Epilogue: the SumIT tile is transposed through shared memory so that
-//     lane L handles shifts x0 + 32*m + L; the eight corner loads per shift
-//     and the fp32 stores are then coalesced across the warp.  num and vI
-//     are exact int64; they are converted to fp32 through two 32-bit halves
-//     (the 64-bit convert runs on the slow fp64 pipe on this part).
+//   - Epilogue: the SumIT tile is transposed through shared memory; the CTA
+//     then walks its output rows two at a time (warps 0-3 one row, warps 4-7
+//     the next), one shift per thread.  The four table-row segments a row
+//     needs (S and Q at rows y-1 and y+hT-1, columns x0-2 .. x0+wT+127)
+//     arrive by TMA into a two-stage shared-memory ring; the first stages
+//     are issued before the numerator loop, so their latency hides behind
+//     it.  TMA's zero fill outside the tables implements the four-corner
+//     rule's row -1 / column -1 = 0.  (Tables whose rows are not a multiple
+//     of 16 bytes, or templates wider than 127, read the corners with
+//     coalesced global loads instead.)  num and vI are exact int64; they
+//     become fp32 through two 32-bit halves (the 64-bit convert runs on the
+//     slow fp64 pipe on this part).
 #include "ncc_common.cuh"
 
 #include <cuda.h>
@@ -46,12 +53,19 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kMaxTmaBox = 256;        // TMA box extent limit per dimension
 constexpr int kMaxSmem = 227 * 1024;   // opt-in shared memory per CTA
 
+constexpr int kEpiStages = 2;          // table-row staging ring depth
+constexpr int kEpiRowsPerStep = 2;     // output rows per epilogue step
+constexpr int kEpiBufs = 4 * kEpiRowsPerStep;  // S/Q x top/bottom x rows
+
 struct Geom {
     int nch;         // 16-pixel template chunks
     int boxW;        // staged tile width in bytes = kOutW + 16*nch
     int boxH;        // staged tile height = kOutH + hT - 1
     int copyStride;  // bytes between shifted copies
     int tmplOff;     // offset of the packed template
+    int epiBW;       // table-row segment length (int64 elements), even
+    int epiBuf;      // bytes per segment buffer (128-aligned)
+    int epiOff;      // offset of the staging ring
     int smemBytes;   // dynamic shared memory (plus 128 bytes of alignment slack)
 };
 
@@ -63,7 +77,10 @@ Geom make_geom(int wT, int hT) {
     const int copyBytes = g.boxW * g.boxH;
     g.copyStride = (copyBytes + 127) / 128 * 128 + 32;
     g.tmplOff = 4 * g.copyStride;  // >= kOutH*kOutW*4: the SumIT transpose reuses the copies
-    g.smemBytes = g.tmplOff + hT * g.nch * 16 + 128;
+    g.epiBW = (kOutW + wT + 2) & ~1;   // columns x0-2 .. x0+wT+127, rounded up to even
+    g.epiBuf = (g.epiBW * 8 + 127) / 128 * 128;
+    g.epiOff = (g.tmplOff + hT * g.nch * 16 + 127) / 128 * 128;
+    g.smemBytes = g.epiOff + kEpiStages * kEpiBufs * g.epiBuf + 128;
     return g;
 }
 
@@ -97,13 +114,39 @@ __device__ __forceinline__ float i64_to_f32(long long v) {
     return v < 0 ? -f : f;
 }
 
-template <bool kTma, bool kMoments>
+__device__ __forceinline__ void tma_2d(const CUtensorMap *map, void *dst, int x, int y,
+                                       unsigned long long *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Bounded wait on an mbarrier phase; gives up (recording the status) rather
+// than hang if a transfer never lands.
+__device__ __forceinline__ void mbar_wait(unsigned long long *bar, uint32_t parity, int *status) {
+    uint32_t done = 0;
+    for (unsigned it = 0; !done; ++it) {
+        asm volatile(
+            "{ .reg .pred P; mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2; selp.u32 %0, 1, 0, P; }"
+            : "=r"(done) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+        if (it > (1u << 24)) {
+            record_status(status, NCC_ERR_TIMEOUT);
+            break;
+        }
+    }
+}
+
+template <bool kTma, bool kMoments, bool kTmaEpi>
 __global__ void __launch_bounds__(kThreads, 3)
-corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const KParams p) {
+corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmS,
+                 const __grid_constant__ CUtensorMap tmQ, const KParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     __shared__ __align__(8) unsigned long long s_bar;
+    __shared__ __align__(8) unsigned long long s_ebar[kEpiStages];
     __shared__ unsigned s_red[kWarps][2];
     __shared__ long long s_sumT, s_vT;
     __shared__ float s_invSqrtVT;
@@ -111,6 +154,32 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const KParams p) {
     const Geom &g = p.g;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int x0 = blockIdx.x * kOutW, y0 = blockIdx.y * kOutH;
+    const int epiSteps = min(kOutH, p.Oy - y0 + kEpiRowsPerStep - 1) / kEpiRowsPerStep;
+    uint8_t *epi = smem + g.epiOff;
+    // table-row segments of epilogue step t: rows y0+2t+h, buffers
+    // [stage][h][S top, S bottom, Q top, Q bottom]
+    auto issue_epi = [&](int t) {
+        const int st = t % kEpiStages;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                     ::"r"(smem_u32(&s_ebar[st])), "r"((uint32_t)(kEpiBufs * g.epiBW * 8))
+                     : "memory");
+        for (int h = 0; h < kEpiRowsPerStep; ++h) {
+            const int y = y0 + kEpiRowsPerStep * t + h;
+            uint8_t *b = epi + (st * kEpiBufs + 4 * h) * g.epiBuf;
+            tma_2d(&tmS, b, x0 - 2, y - 1, &s_ebar[st]);
+            tma_2d(&tmS, b + g.epiBuf, x0 - 2, y + p.hT - 1, &s_ebar[st]);
+            tma_2d(&tmQ, b + 2 * g.epiBuf, x0 - 2, y - 1, &s_ebar[st]);
+            tma_2d(&tmQ, b + 3 * g.epiBuf, x0 - 2, y + p.hT - 1, &s_ebar[st]);
+        }
+    };
+
+    if (kTmaEpi && tid == 0) {
+        for (int i = 0; i < kEpiStages; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_ebar[i])));
+        asm volatile("fence.mbarrier_init.release.cluster;");
+        asm volatile("fence.proxy.async.shared::cta;");
+        for (int t = 0; t < kEpiStages && t < epiSteps; ++t) issue_epi(t);
+    }
 
     // --- stage the image tile (copy 0) ---------------------------------
     if (kTma) {
@@ -170,19 +239,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const KParams p) {
         s_vT = vT;
         s_invSqrtVT = vT > 0 ? __frsqrt_rn(u64_to_f32((unsigned long long)vT)) : 0.0f;
     }
-    if (kTma) {
-        // every thread waits for the TMA transaction to land (bounded)
-        uint32_t done = 0;
-        for (unsigned it = 0; !done; ++it) {
-            asm volatile(
-                "{ .reg .pred P; mbarrier.try_wait.parity.shared::cta.b64 P, [%1], 0; selp.u32 %0, 1, 0, P; }"
-                : "=r"(done) : "r"(smem_u32(&s_bar)) : "memory");
-            if (it > (1u << 24)) {
-                record_status(p.status, NCC_ERR_TIMEOUT);
-                break;
-            }
-        }
-    }
+    if (kTma) mbar_wait(&s_bar, 0, p.status);  // every thread: the tile has landed
     __syncthreads();
 
     // --- byte-shifted copies 1..3 -----------------------------------------
@@ -238,33 +295,43 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const KParams p) {
 
     // --- transpose SumIT through shared memory ------------------------------
     __syncthreads();  // every warp is done with the staged copies
-    uint32_t *sIT = reinterpret_cast<uint32_t *>(smem) + warp * kRowsPerThread * kOutW;
+    uint32_t *sIT = reinterpret_cast<uint32_t *>(smem);  // [kOutH][kOutW]
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sIT[i * kOutW + 16 * qg + 4 * k + d] = acc[i][k];
-    __syncwarp();
+        for (int k = 0; k < 4; ++k)
+            sIT[(warp * kRowsPerThread + i) * kOutW + 16 * qg + 4 * k + d] = acc[i][k];
+    __syncthreads();
 
     // --- epilogue: moments from S and Q, coefficient -----------------------
     const long long N = (long long)p.wT * p.hT;
     const long long sT = s_sumT, vT = s_vT;
     const float invSqrtVT = s_invSqrtVT;
-    const size_t W = (size_t)p.W;
-    for (int i = 0; i < kRowsPerThread; ++i) {
-        const int y = y0 + warp * kRowsPerThread + i;
-        if (y >= p.Oy) break;
-        const long long *St = p.S + (size_t)(y - 1) * W, *Sb = p.S + (size_t)(y + p.hT - 1) * W;
-        const long long *Qt = p.Q + (size_t)(y - 1) * W, *Qb = p.Q + (size_t)(y + p.hT - 1) * W;
-#pragma unroll 2
-        for (int m = 0; m < 4; ++m) {
-            const int xo = 32 * m + lane, x = x0 + xo;
-            if (x >= p.Ox) break;
+    const int h = warp >> 2, xo = (warp & 3) * 32 + lane, x = x0 + xo;
+    for (int t = 0; t < epiSteps; ++t) {
+        const int row = kEpiRowsPerStep * t + h, y = y0 + row;
+        long long sI = 0, sI2 = 0;
+        if (kTmaEpi) {
+            mbar_wait(&s_ebar[t % kEpiStages], (uint32_t)((t / kEpiStages) & 1), p.status);
+            const long long *b = reinterpret_cast<const long long *>(
+                epi + ((t % kEpiStages) * kEpiBufs + 4 * h) * g.epiBuf);
+            const int stride = g.epiBuf / 8;
+            const int cl = xo + 1, cr = xo + p.wT + 1;  // columns x-1 and x+wT-1 from x0-2
+            sI = b[stride + cr] - b[cr] - b[stride + cl] + b[cl];
+            sI2 = b[3 * stride + cr] - b[2 * stride + cr] - b[3 * stride + cl] + b[2 * stride + cl];
+        } else if (y < p.Oy && x < p.Ox) {
+            const size_t W = (size_t)p.W;
+            const long long *St = p.S + (size_t)(y - 1) * W, *Sb = p.S + (size_t)(y + p.hT - 1) * W;
+            const long long *Qt = p.Q + (size_t)(y - 1) * W, *Qb = p.Q + (size_t)(y + p.hT - 1) * W;
             const int xl = x - 1, xr = x + p.wT - 1;
-            long long sI = __ldg(Sb + xr), sI2 = __ldg(Qb + xr);
+            sI = __ldg(Sb + xr);
+            sI2 = __ldg(Qb + xr);
             if (y > 0) { sI -= __ldg(St + xr); sI2 -= __ldg(Qt + xr); }
             if (x > 0) { sI -= __ldg(Sb + xl); sI2 -= __ldg(Qb + xl); }
             if (x > 0 && y > 0) { sI += __ldg(St + xl); sI2 += __ldg(Qt + xl); }
-            const unsigned sumIT = sIT[i * kOutW + xo];
+        }
+        if (y < p.Oy && x < p.Ox) {
+            const unsigned sumIT = sIT[row * kOutW + xo];
             const size_t o = (size_t)y * p.Ox + x;
             if (kMoments) {
                 p.sumI[o] = sI;
@@ -283,6 +350,10 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const KParams p) {
                 }
                 __stcs(p.out + o, r);
             }
+        }
+        if (kTmaEpi) {
+            __syncthreads();  // stage (t % kEpiStages) is free again
+            if (tid == 0 && t + kEpiStages < epiSteps) issue_epi(t + kEpiStages);
         }
     }
 }
@@ -347,21 +418,50 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
         tma = false;
     }
     const bool moments = a.sumIT != nullptr;
+    CUtensorMap tmS, tmQ;
+    memset(&tmS, 0, sizeof(tmS));
+    memset(&tmQ, 0, sizeof(tmQ));
+    bool tmaEpi = (a.W % 2 == 0) && ((uintptr_t)a.S % 16 == 0) && ((uintptr_t)a.Q % 16 == 0) &&
+                  p.g.epiBW <= kMaxTmaBox;
+    if (tmaEpi) enc = encode_fn();
+    if (tmaEpi && enc) {
+        const cuuint64_t dims[2] = {(cuuint64_t)a.W, (cuuint64_t)a.H};
+        const cuuint64_t strides[1] = {(cuuint64_t)a.W * 8};
+        const cuuint32_t box[2] = {(cuuint32_t)p.g.epiBW, 1};
+        const cuuint32_t estr[2] = {1, 1};
+        CUresult r1 = enc(&tmS, CU_TENSOR_MAP_DATA_TYPE_INT64, 2, const_cast<int64_t *>(a.S), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        CUresult r2 = enc(&tmQ, CU_TENSOR_MAP_DATA_TYPE_INT64, 2, const_cast<int64_t *>(a.Q), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        tmaEpi = (r1 == CUDA_SUCCESS && r2 == CUDA_SUCCESS);
+    } else {
+        tmaEpi = false;
+    }
     const dim3 grid((p.Ox + kOutW - 1) / kOutW, (p.Oy + kOutH - 1) / kOutH);
     const dim3 block(kThreads);
     const size_t smem = (size_t)p.g.smemBytes;
     cudaError_t e;
-#define NCC_LAUNCH(T, M)                                                                     \
+#define NCC_LAUNCH(T, M, E)                                                                  \
     do {                                                                                     \
-        e = cudaFuncSetAttribute(corr_dp4a_kernel<T, M>,                                     \
+        e = cudaFuncSetAttribute(corr_dp4a_kernel<T, M, E>,                                  \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);    \
         if (e != cudaSuccess) return e;                                                      \
-        corr_dp4a_kernel<T, M><<<grid, block, smem, stream>>>(tmap, p);                      \
+        corr_dp4a_kernel<T, M, E><<<grid, block, smem, stream>>>(tmap, tmS, tmQ, p);         \
     } while (0)
-    if (tma && moments) NCC_LAUNCH(true, true);
-    else if (tma) NCC_LAUNCH(true, false);
-    else if (moments) NCC_LAUNCH(false, true);
-    else NCC_LAUNCH(false, false);
+#define NCC_LAUNCH_E(T, M)                    \
+    do {                                      \
+        if (tmaEpi) NCC_LAUNCH(T, M, true);   \
+        else NCC_LAUNCH(T, M, false);         \
+    } while (0)
+    if (tma && moments) NCC_LAUNCH_E(true, true);
+    else if (tma) NCC_LAUNCH_E(true, false);
+    else if (moments) NCC_LAUNCH_E(false, true);
+    else NCC_LAUNCH_E(false, false);
+#undef NCC_LAUNCH_E
 #undef NCC_LAUNCH
     return cudaGetLastError();
 }
