@@ -31,6 +31,7 @@ from normalized_cross_correlation_gb300 import inputs  # noqa: E402
 
 METRIC = "NCC coefficients/s (4096², 16×16 tmpl); SAT build GB/s vs HBM peak"
 UNIT = "coefficients/s"
+DEFAULT_WORKLOAD = "ncc_4096_t16"
 SAT_BYTES_PER_PX = 17          # 1 B read + 8 B (S) + 8 B (Q) written per pixel
 CORR_BYTES_PER_COEFF = 21      # S and Q corners (16 B after reuse) + 1 B image + 4 B out
 L2_FLUSH_BYTES = 512 << 20     # > 129 MB L2
@@ -128,13 +129,21 @@ def oracle_sample_rate(w: inputs.Workload, band_rows: int, threads: int) -> tupl
     oracle.sat(sub)
     oracle.correlate(sub, w.templates, threads=threads)
     dt = time.perf_counter() - t0
-    return band_rows * w.Ox / dt, dt
+    return w.nT * band_rows * w.Ox / dt, dt
+
+
+def sample_rows(w: inputs.Workload, requested: int | None) -> int:
+    """Output rows of the oracle's bounded sample: the request, else as many
+    rows as fit about 2e10 multiply-adds (a few seconds on many cores)."""
+    if requested:
+        return max(1, min(requested, w.Oy))
+    return max(1, min(w.Oy, int(2e10 // (w.nT * w.Ox * w.wT * w.hT))))
 
 
 def run_reference(args, w: inputs.Workload) -> dict:
     import oracle
     threads = oracle.default_threads()
-    band = args.ref_rows
+    band = sample_rows(w, args.ref_rows)
     for _ in range(args.warmup):
         oracle_sample_rate(w, band, threads)
     times = []
@@ -142,16 +151,16 @@ def run_reference(args, w: inputs.Workload) -> dict:
         _, dt = oracle_sample_rate(w, band, threads)
         times.append(dt)
     per_step = statistics.mean(times)
-    rate = band * w.Ox / per_step
-    sample = (f"tables of the top {band + w.hT - 1} image rows + all {band}x{w.Ox} "
+    rate = w.nT * band * w.Ox / per_step
+    sample = (f"tables of the top {band + w.hT - 1} image rows + all {w.nT}x{band}x{w.Ox} "
               f"coefficients of those rows, per step")
     return {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": w.name, "image": "4096x4096 u8", "template": "16x16 u8",
-                   "sample_rows": band},
+        "config": {"workload": w.name, "image": f"{w.W}x{w.H} u8",
+                   "templates": f"{w.nT}x{w.hT}x{w.wT} u8", "sample_rows": band},
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -168,25 +177,33 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    ncc.lib()
+    L = ncc.lib()
     stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
     dev = torch.device("cuda", local)
 
+    nT = w.nT
     img = torch.from_numpy(w.image).to(dev)
-    tmpl = torch.from_numpy(w.templates[0]).to(dev)
     S = torch.empty((w.H, w.W), dtype=torch.int64, device=dev)
     Q = torch.empty((w.H, w.W), dtype=torch.int64, device=dev)
-    out = torch.empty((w.Oy, w.Ox), dtype=torch.float32, device=dev)
+    if nT:
+        tmpl = torch.from_numpy(w.templates).to(dev)
+        out = torch.empty((nT, w.Oy, w.Ox), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    L = ncc.lib()
-    sh = stream.cuda_stream
+    ev_mid = None
 
     def step():
         rc = L.ncc_sat_build(img.data_ptr(), w.W, w.H, S.data_ptr(), Q.data_ptr(), sh)
         assert rc == 0, rc
+        if not nT:
+            return
         ev_mid.record(stream)
-        rc = L.ncc_correlate(img.data_ptr(), w.W, w.H, tmpl.data_ptr(), w.wT, w.hT,
-                             S.data_ptr(), Q.data_ptr(), out.data_ptr(), sh)
+        if nT == 1:
+            rc = L.ncc_correlate(img.data_ptr(), w.W, w.H, tmpl.data_ptr(), w.wT, w.hT,
+                                 S.data_ptr(), Q.data_ptr(), out.data_ptr(), sh)
+        else:
+            rc = L.ncc_correlate_bank(img.data_ptr(), w.W, w.H, tmpl.data_ptr(), w.wT, w.hT, nT,
+                                      S.data_ptr(), Q.data_ptr(), out.data_ptr(), sh)
         assert rc == 0, rc
 
     ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -209,6 +226,8 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
             ev_a[k].record(stream)
             ev_mid = ev_m[k]
             step()
+            if not nT:
+                ev_m[k].record(stream)
             ev_b[k].record(stream)
         torch.cuda.synchronize()
         if dist is not None:
@@ -222,27 +241,32 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
         t = torch.tensor([ms_step], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_step = float(t.item())
-    coeffs = w.Ox * w.Oy
+    coeffs = nT * w.Ox * w.Oy if nT else w.W * w.H
     value = ws * coeffs / (ms_step * 1e-3)
 
     # end to end through the host-buffer entry point (pinned host memory)
-    himg = torch.from_numpy(w.image).pin_memory()
-    htmp = torch.from_numpy(w.templates).pin_memory()
-    hout = torch.empty((1, w.Oy, w.Ox), dtype=torch.float32).pin_memory()
-    e2e_steps = max(3, min(args.steps, 10))
-    for _ in range(2):
-        ncc.ncc_match_host(himg, htmp, hout)
-    e2e_t = []
-    for _ in range(e2e_steps):
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        ncc.ncc_match_host(himg, htmp, hout)      # synchronizes the stream
-        e2e_t.append(time.perf_counter() - t0)
-    e2e_ms = statistics.mean(e2e_t) * 1e3
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e = None
+    if nT:
+        himg = torch.from_numpy(w.image).pin_memory()
+        htmp = torch.from_numpy(w.templates).pin_memory()
+        hout = torch.empty((nT, w.Oy, w.Ox), dtype=torch.float32).pin_memory()
+        e2e_steps = max(3, min(args.steps, 10))
+        for _ in range(2):
+            ncc.ncc_match_host(himg, htmp, hout)
+        e2e_t = []
+        for _ in range(e2e_steps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            ncc.ncc_match_host(himg, htmp, hout)      # synchronizes the stream
+            e2e_t.append(time.perf_counter() - t0)
+        e2e_ms = statistics.mean(e2e_t) * 1e3
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": ws * coeffs / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": int(w.image.nbytes + w.templates.nbytes),
+               "d2h_bytes_per_step": int(coeffs * 4)}
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -253,46 +277,67 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
     hbm = float(peaks["hbm_gbs"])
     sat_ms, corr_ms = statistics.mean(t_sat), statistics.mean(t_corr)
     sat_gbs = SAT_BYTES_PER_PX * w.W * w.H / (sat_ms * 1e-3) / 1e9
-    corr_gbs = CORR_BYTES_PER_COEFF * coeffs / (corr_ms * 1e-3) / 1e9
-    dp4a = coeffs * ((w.wT + 3) // 4) * w.hT
-    alu_peak = DP4A_PER_SM_CLK * N_SMS * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
     roof_sat = {"kernel": "sat_build", "bound": "hbm", "achieved": sat_gbs, "peak": hbm,
                 "unit": "GB/s", "frac": sat_gbs / hbm, "traffic": None,
                 "peak_source": peaks["source"]}
-    roof_corr_alu = {"kernel": "corr_dp4a", "bound": "alu", "achieved": dp4a / (corr_ms * 1e-3) / 1e12,
-                     "peak": alu_peak / 1e12, "unit": "Tdp4a/s",
-                     "frac": dp4a / (corr_ms * 1e-3) / alu_peak, "traffic": None}
-    roof_corr_hbm = {"kernel": "corr_dp4a", "bound": "hbm", "achieved": corr_gbs, "peak": hbm,
-                     "unit": "GB/s", "frac": corr_gbs / hbm, "traffic": None}
-    corr_roof = max(roof_corr_alu, roof_corr_hbm, key=lambda r: r["frac"])
-    dominant = roof_sat if sat_ms >= corr_ms else corr_roof
+    rooflines = [roof_sat]
+    corr = None
+    dominant = roof_sat
+    if nT:
+        macs = coeffs * w.wT * w.hT
+        if nT == 1:
+            # S and Q corners (16 B after reuse) + 1 B image + 4 B out per coefficient
+            corr_bytes = 21 * w.Ox * w.Oy
+            dp4a = w.Ox * w.Oy * ((w.wT + 3) // 4) * w.hT
+            alu_peak = DP4A_PER_SM_CLK * N_SMS * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+            r2 = {"kernel": "corr_dp4a", "bound": "alu",
+                  "achieved": dp4a / (corr_ms * 1e-3) / 1e12, "peak": alu_peak / 1e12,
+                  "unit": "Tdp4a/s", "frac": dp4a / (corr_ms * 1e-3) / alu_peak, "traffic": None}
+        else:
+            # 4 B out per coefficient + S and Q (16 B) + image (1 B) per shift
+            corr_bytes = 4 * coeffs + 17 * w.Ox * w.Oy
+            tflops = 2.0 * macs / (corr_ms * 1e-3) / 1e12
+            peak_tc = float(peaks.get("bf16_tflops", 1900.0))  # f16 runs at the bf16 rate
+            r2 = {"kernel": "bank_tc", "bound": "tensor", "achieved": tflops, "peak": peak_tc,
+                  "unit": "TFLOP/s", "frac": tflops / peak_tc, "traffic": None}
+        corr_gbs = corr_bytes / (corr_ms * 1e-3) / 1e9
+        r1 = {"kernel": r2["kernel"], "bound": "hbm", "achieved": corr_gbs, "peak": hbm,
+              "unit": "GB/s", "frac": corr_gbs / hbm, "traffic": None}
+        rooflines += [r1, r2]
+        corr_roof = max(r1, r2, key=lambda r: r["frac"])
+        dominant = roof_sat if sat_ms >= corr_ms else corr_roof
+        corr = {"kernel": r2["kernel"], "ms": corr_ms, "GB/s": corr_gbs,
+                "GMAC/s": macs / (corr_ms * 1e-3) / 1e9}
 
     cpu = None
-    if args.cpu_baseline:
+    if args.cpu_baseline and nT and rank == 0:
         import oracle
         threads = oracle.default_threads()
-        rate, dt = oracle_sample_rate(w, args.ref_rows, threads)
-        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"tables of the top {args.ref_rows + w.hT - 1} image rows + all "
-                         f"{args.ref_rows}x{w.Ox} coefficients of those rows ({dt:.1f} s)"}
+        rows = sample_rows(w, args.ref_rows)
+        rate, dt = oracle_sample_rate(w, rows, threads)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads,
+               "kind": "oracle",
+               "sample": f"tables of the top {rows + w.hT - 1} image rows + all "
+                         f"{nT}x{rows}x{w.Ox} coefficients of those rows ({dt:.1f} s)"}
 
+    metric = METRIC if w.name == DEFAULT_WORKLOAD else f"NCC coefficients/s ({w.name})"
     return {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": w.name, "image": "4096x4096 u8 uniform (seed 2)",
-                   "template": "16x16 u8 crop", "step": "ncc_sat_build + ncc_correlate",
+        "metric": metric, "value": value, "unit": UNIT if nT else "pixels/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic",
+        "config": {"workload": w.name, "image": f"{w.W}x{w.H} u8",
+                   "templates": f"{nT}x{w.hT}x{w.wT} u8" if nT else None,
+                   "step": "ncc_sat_build + " + ("ncc_correlate" if nT == 1 else
+                                                 "ncc_correlate_bank" if nT else "nothing"),
                    "l2": "flushed between timed steps (512 MB write)"},
         "sat_build": {"ms": sat_ms, "GB/s": sat_gbs, "frac_of_hbm": sat_gbs / hbm},
-        "correlate": {"ms": corr_ms, "GB/s": corr_gbs, "Tdp4a/s": roof_corr_alu["achieved"],
-                      "GMAC/s": coeffs * w.wT * w.hT / (corr_ms * 1e-3) / 1e9},
+        "correlate": corr,
         "roofline": {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")},
-        "rooflines": [roof_sat, roof_corr_hbm, roof_corr_alu],
+        "rooflines": rooflines,
         "cpu_baseline": cpu,
-        "e2e": {"value": ws * coeffs / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": int(w.image.nbytes + w.templates.nbytes),
-                "d2h_bytes_per_step": int(coeffs * 4)},
-        "gpu_launches": 2 * args.steps,
+        "e2e": e2e,
+        "gpu_launches": (2 if nT else 1) * args.steps,
         "clocks": clocks.summary(),
     }
 
@@ -303,16 +348,19 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--ref-rows", type=int, default=4081,
-                    help="output rows of the oracle's bounded sample per step")
+    ap.add_argument("--ref-rows", type=int, default=None,
+                    help="output rows of the oracle's bounded sample per step "
+                         "(default: about 2e10 multiply-adds' worth)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.NAMED),
+                    help="workload to time (the default is the headline metric's)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "gb300" else args.warmup
 
-    w = inputs.headline_4096()
+    w = inputs.NAMED[args.workload]()
     ws, rank, _ = dist_env()
     if args.impl == "reference":
-        if rank != 0:
+        if rank != 0 or not w.nT:
             return
         print(json.dumps(run_reference(args, w)), flush=True)
         return

@@ -27,9 +27,15 @@
 //              commits (tcgen05.commit -> mbarrier),
 //   warps 1-3  convert image rows (u8 -> f16 shifted copies) into a ring of
 //              A buffers in shared memory,
-//   warps 4-7  epilogue: tcgen05.ld one accumulator row per thread (thread
-//              = shift), box sums from S and Q once per shift, exact int64
-//              num and vI, fp32 coefficient per template, coalesced stores.
+//   warps 4-11 epilogue: two warps per tensor-memory lane quarter (one per
+//              half of the template columns); tcgen05.ld of the accumulator
+//              row of its shift, box sums from S and Q once per shift
+//              (prefetched a row ahead), the coefficient of every template
+//              and coalesced fp32 stores.  With one exact fp32 group the
+//              numerator N*SumIT - SumI*SumT is formed without rounding
+//              error before its final rounding: both products are split
+//              exactly by fma and their high parts cancel exactly
+//              (Sterbenz) whenever the difference is small.
 // All hand-offs are mbarriers; every wait is bounded and a wait that runs out
 // records NCC_ERR_TIMEOUT and lets the CTA finish (never a hang).
 #include "ncc_common.cuh"
@@ -39,17 +45,18 @@
 namespace ncc {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kM = 128;               // shifts per tile (MMA M)
 constexpr int kTY = 32;               // output rows per tile
 constexpr int kProducers = 96;        // warps 1-3
-constexpr int kEpi0 = 128;            // first epilogue thread (warps 4-7)
+constexpr int kEpi0 = 128;            // first epilogue thread (warps 4-11)
+constexpr int kEpiThreads = kThreads - kEpi0;
 constexpr int kMaxExactPixels = 258;  // 258 * 255^2 < 2^24: exact fp32 accumulation
 constexpr int kMaxSmem = 110 * 1024;  // two CTAs per SM
 constexpr int kMaxTmemCols = 256;     // per CTA (two CTAs share 512 columns)
 
 struct BankGeom {
-    int nTpad;      // templates padded to a multiple of 16 (MMA N)
+    int nTpad;      // templates padded to a multiple of 32 (MMA N; 32-column TMEM loads)
     int nK16;       // 16-column template chunks (MMA K steps per template row)
     int G;          // template rows per exact accumulator group
     int nG;         // groups
@@ -71,7 +78,7 @@ int pow2_at_least(int v) {
 
 bool make_geom(int wT, int hT, int nT, BankGeom &g) {
     if (wT > kMaxExactPixels) return false;
-    g.nTpad = (nT + 15) / 16 * 16;
+    g.nTpad = (nT + 31) / 32 * 32;
     if (g.nTpad > 256) return false;
     g.nK16 = (wT + 15) / 16;
     g.G = kMaxExactPixels / wT;
@@ -90,7 +97,7 @@ bool make_geom(int wT, int hT, int nT, BankGeom &g) {
     g.offB = 0;
     g.offX = (g.bBytes + 1023) / 1024 * 1024;
     g.offSt = g.offX + g.nx * g.xBytes;
-    const int stBytes = g.nTpad * (8 + 8 + 4);
+    const int stBytes = g.nTpad * 8;   // float2 {SumT, 1/sqrt(vT)} per template
     g.offBar = (g.offSt + stBytes + 15) / 16 * 16;
     const int barBytes = (2 * g.nx + 2 * g.na) * 8 + 16;
     g.smemBytes = g.offBar + barBytes + 1024;  // + alignment slack
@@ -141,8 +148,11 @@ __device__ __forceinline__ void mbar_arrive(unsigned long long *b) {
 // that runs out, *abort short-circuits every later wait of the CTA.
 __device__ __forceinline__ void mbar_wait(unsigned long long *b, uint32_t parity, int *abort,
                                           int *status) {
-    if (*(volatile int *)abort) return;
     uint32_t done = 0;
+    asm volatile(
+        "{ .reg .pred P; mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2; selp.u32 %0, 1, 0, P; }"
+        : "=r"(done) : "r"(saddr(b)), "r"(parity) : "memory");
+    if (done || *(volatile int *)abort) return;  // fast path: no timer read
     const uint64_t t0 = global_timer_ns();
     for (unsigned it = 0; !done; ++it) {
         asm volatile(
@@ -192,7 +202,7 @@ __device__ __forceinline__ uint32_t bytes_to_h2(uint32_t w, uint32_t sel) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <bool kMoments>
+template <bool kMoments, bool kOneGroup>
 __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -202,9 +212,7 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
     const BankGeom &g = p.g;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    int *sT = reinterpret_cast<int *>(smem + g.offSt);                        // [nTpad]
-    long long *vT = reinterpret_cast<long long *>(smem + g.offSt + 4 * g.nTpad);  // [nTpad]
-    float *invs = reinterpret_cast<float *>(smem + g.offSt + 12 * g.nTpad);   // [nTpad]
+    float2 *sts = reinterpret_cast<float2 *>(smem + g.offSt);  // [nTpad] {SumT, 1/sqrt(vT)}
     unsigned long long *bar = reinterpret_cast<unsigned long long *>(smem + g.offBar);
     unsigned long long *xfull = bar, *xempty = bar + g.nx;
     unsigned long long *afull = bar + 2 * g.nx, *aempty = afull + g.na;
@@ -237,13 +245,12 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                 }
             }
             const long long v2 = N * (long long)b - (long long)a * (long long)a;
-            sT[n] = (int)a;
-            vT[n] = v2;
-            invs[n] = (n < p.nT && v2 > 0) ? __frsqrt_rn(u64_to_f32((unsigned long long)v2)) : 0.f;
+            sts[n] = make_float2((float)a,  // SumT < 2^25: exact
+                                 (n < p.nT && v2 > 0) ? __frsqrt_rn(u64_to_f32((unsigned long long)v2)) : 0.f);
         }
         if (tid == 0) {
             for (int i = 0; i < g.nx; ++i) { mbar_init(&xfull[i], kProducers); mbar_init(&xempty[i], 1); }
-            for (int i = 0; i < g.na; ++i) { mbar_init(&afull[i], 1); mbar_init(&aempty[i], kThreads - kEpi0); }
+            for (int i = 0; i < g.na; ++i) { mbar_init(&afull[i], 1); mbar_init(&aempty[i], kEpiThreads); }
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             s_abort = 0;
         }
@@ -298,96 +305,128 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
             }
         } else if (warp == 0) {
             // ---- MMA issuer ----
+            // Descriptors are linear in the shared address (field = addr >> 4),
+            // so the loop only adds precomputed steps: no divisions per MMA.
             if (lane == 0) {
+                const uint64_t adesc0 = smem_desc(saddr(smem + g.offX), 128, 128);
+                const uint64_t bdesc0 = smem_desc(saddr(smem + g.offB), g.nTpad * 16, 128);
+                const uint32_t xStep = (uint32_t)g.xBytes >> 4;                 // next A buffer
+                const uint32_t bRow = (uint32_t)(g.nK16 * g.nTpad * 32) >> 4;  // next template row
+                const uint32_t bChunk = (uint32_t)(g.nTpad * 32) >> 4;         // next K chunk
+                const uint32_t slot0 = rowSeq % g.nx;                           // slot of image row y0
+                uint32_t readySlot = slot0;
                 int ready = 0;  // image rows of this tile known to be converted
                 for (int yl = 0; yl < ty; ++yl) {
                     const uint32_t o = outSeq + yl, a = o % g.na, ka = o / g.na;
                     if (ka > 0) mbar_wait(&aempty[a], (ka - 1) & 1, &s_abort, p.status);
                     while (ready < yl + p.hT) {
                         const uint32_t q = rowSeq + ready;
-                        mbar_wait(&xfull[q % g.nx], (q / g.nx) & 1, &s_abort, p.status);
+                        mbar_wait(&xfull[readySlot], (q / g.nx) & 1, &s_abort, p.status);
                         ++ready;
+                        if (++readySlot == (uint32_t)g.nx) readySlot = 0;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint32_t d = tmem + a * g.accCols;
+                    uint32_t s = (slot0 + yl) % g.nx;  // slot of image row y0+yl
+                    uint32_t d = tmem + a * g.accCols;
+                    uint64_t bd = bdesc0;
+                    int inGroup = 0;
                     for (int j = 0; j < p.hT; ++j) {
-                        const uint32_t q = rowSeq + yl + j;
-                        const uint32_t xa = saddr(smem + g.offX + (q % g.nx) * g.xBytes);
-                        const uint32_t ba = saddr(smem + g.offB + j * g.nK16 * g.nTpad * 32);
-                        const int grp = j / g.G;
-                        for (int c = 0; c < g.nK16; ++c) {
-                            const uint64_t ad = smem_desc(xa + 256 * c, 128, 128);
-                            const uint64_t bd = smem_desc(ba + c * g.nTpad * 32, g.nTpad * 16, 128);
-                            tc_mma(d + grp * g.nTpad, ad, bd, idesc, (j % g.G != 0 || c != 0) ? 1u : 0u);
-                        }
+                        const uint64_t ad = adesc0 + (uint64_t)(s * xStep);
+                        for (int c = 0; c < g.nK16; ++c)
+                            tc_mma(d, ad + 16u * c, bd + c * bChunk, idesc,
+                                   (inGroup != 0 || c != 0) ? 1u : 0u);
+                        bd += bRow;
+                        if (++s == (uint32_t)g.nx) s = 0;
+                        if (++inGroup == g.G) { inGroup = 0; d += g.nTpad; }
                     }
                     tc_commit(&afull[a]);
-                    tc_commit(&xempty[(rowSeq + yl) % g.nx]);  // image row y0+yl is done
+                    tc_commit(&xempty[(slot0 + yl) % g.nx]);  // image row y0+yl is done
                 }
-                for (int rl = ty; rl < nrows; ++rl) tc_commit(&xempty[(rowSeq + rl) % g.nx]);
+                for (int rl = ty; rl < nrows; ++rl) tc_commit(&xempty[(slot0 + rl) % g.nx]);
             }
             __syncwarp();
         } else {
-            // ---- epilogue: thread = shift x0 + et ----
-            const int et = tid - kEpi0;
-            const int x = x0 + et;
-            const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+            // ---- epilogue: thread = shift x0 + 32*sp + lane, template chunks ci = ch (mod 2) ----
+            const int sp = warp & 3, ch = (warp - 4) >> 2;
+            const int x = x0 + 32 * sp + lane;
+            const uint32_t lane_base = (uint32_t)(32 * sp) << 16;
             const bool xin = x < p.Ox;
+            const size_t W = (size_t)p.W, plane = (size_t)p.Oy * p.Ox;
+            const int xl = x - 1, xr = x + p.wT - 1;
+            const float Nf = (float)N;  // < 2^17: exact
+            long long cS[4], cQ[4];     // corners of the current row: br, tr, bl, tl
+            auto load_corners = [&](int y) {
+                const int yt = y - 1, ybm = y + p.hT - 1;
+                cS[0] = cS[1] = cS[2] = cS[3] = 0;
+                cQ[0] = cQ[1] = cQ[2] = cQ[3] = 0;
+                if (!xin) return;
+                cS[0] = __ldg(p.S + (size_t)ybm * W + xr);
+                cQ[0] = __ldg(p.Q + (size_t)ybm * W + xr);
+                if (yt >= 0) { cS[1] = __ldg(p.S + (size_t)yt * W + xr); cQ[1] = __ldg(p.Q + (size_t)yt * W + xr); }
+                if (xl >= 0) { cS[2] = __ldg(p.S + (size_t)ybm * W + xl); cQ[2] = __ldg(p.Q + (size_t)ybm * W + xl); }
+                if (xl >= 0 && yt >= 0) { cS[3] = __ldg(p.S + (size_t)yt * W + xl); cQ[3] = __ldg(p.Q + (size_t)yt * W + xl); }
+            };
+            load_corners(y0);
             for (int yl = 0; yl < ty; ++yl) {
                 const int y = y0 + yl;
                 const uint32_t o = outSeq + yl, a = o % g.na, ka = o / g.na;
-                long long sI = 0, sI2 = 0;
-                if (xin) {
-                    const size_t W = (size_t)p.W;
-                    const int xl = x - 1, xr = x + p.wT - 1, yt = y - 1, ybm = y + p.hT - 1;
-                    sI = __ldg(p.S + (size_t)ybm * W + xr);
-                    sI2 = __ldg(p.Q + (size_t)ybm * W + xr);
-                    if (yt >= 0) { sI -= __ldg(p.S + (size_t)yt * W + xr); sI2 -= __ldg(p.Q + (size_t)yt * W + xr); }
-                    if (xl >= 0) { sI -= __ldg(p.S + (size_t)ybm * W + xl); sI2 -= __ldg(p.Q + (size_t)ybm * W + xl); }
-                    if (xl >= 0 && yt >= 0) { sI += __ldg(p.S + (size_t)yt * W + xl); sI2 += __ldg(p.Q + (size_t)yt * W + xl); }
-                }
+                const long long sI = cS[0] - cS[1] - cS[2] + cS[3];
+                const long long sI2 = cQ[0] - cQ[1] - cQ[2] + cQ[3];
+                if (yl + 1 < ty) load_corners(y + 1);  // next row's corners, in flight meanwhile
                 const long long vI = (long long)((unsigned long long)N * (unsigned)sI2) -
                                      (long long)((int)sI) * (long long)((int)sI);
                 const float rsI = vI > 0 ? rsqrtf(u64_to_f32((unsigned long long)vI)) : 0.f;
+                const float sIf = (float)(int)sI;  // < 2^25: exact
                 mbar_wait(&afull[a], ka & 1, &s_abort, p.status);
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                if (kMoments && xin) {
-                    const size_t o1 = (size_t)y * p.Ox + x;
-                    p.sumI[o1] = sI;
-                    p.sumI2[o1] = sI2;
+                const size_t obase = (size_t)y * p.Ox + x;
+                if (kMoments && xin && ch == 0) {
+                    p.sumI[obase] = sI;
+                    p.sumI2[obase] = sI2;
                 }
-                for (int cc = 0; cc < g.nTpad; cc += 32) {
-                    uint32_t sum[32];
-                    {
-                        uint32_t v[32];
-                        tc_ld32(tmem + lane_base + a * g.accCols + cc, v);
-                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                for (int ci = ch; ci * 32 < g.nTpad; ci += 2) {
+                    const int cc = 32 * ci;
+                    uint32_t v[32];
+                    tc_ld32(tmem + lane_base + a * g.accCols + cc, v);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                    if (!kOneGroup) {
+                        // several exact groups: sum their integer values
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) sum[i] = __float2uint_rn(__uint_as_float(v[i]));
-                    }
-                    for (int gi = 1; gi < g.nG; ++gi) {
-                        uint32_t v[32];
-                        tc_ld32(tmem + lane_base + a * g.accCols + gi * g.nTpad + cc, v);
-                        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                        for (int i = 0; i < 32; ++i) v[i] = __float2uint_rn(__uint_as_float(v[i]));
+                        for (int gi = 1; gi < g.nG; ++gi) {
+                            uint32_t w[32];
+                            tc_ld32(tmem + lane_base + a * g.accCols + gi * g.nTpad + cc, w);
+                            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) sum[i] += __float2uint_rn(__uint_as_float(v[i]));
-                    }
-                    if (xin) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int t = cc + i;
-                            if (t >= p.nT) continue;
-                            const size_t oo = ((size_t)t * p.Oy + y) * p.Ox + x;
-                            if (kMoments) {
-                                p.sumIT[oo] = (long long)sum[i];
-                            } else {
-                                const long long num = (long long)((unsigned long long)N * sum[i]) -
-                                                      (long long)((int)sI) * (long long)sT[t];
-                                float r = i64_to_f32(num) * rsI * invs[t];
-                                r = fminf(1.0f, fmaxf(-1.0f, r));
-                                __stcs(p.out + oo, r);
-                            }
+                            for (int i = 0; i < 32; ++i) v[i] += __float2uint_rn(__uint_as_float(w[i]));
                         }
+                    }
+                    if (!xin) continue;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int t = cc + i;
+                        if (t >= p.nT) continue;
+                        const size_t oo = obase + (size_t)t * plane;
+                        const float2 st = sts[t];
+                        if (kMoments) {
+                            p.sumIT[oo] = kOneGroup ? (long long)__float2uint_rn(__uint_as_float(v[i]))
+                                                    : (long long)v[i];
+                            continue;
+                        }
+                        float num;
+                        if (kOneGroup) {
+                            // exact N*SumIT - SumI*SumT up to the final rounding
+                            const float sit = __uint_as_float(v[i]);  // exact integer < 2^24
+                            const float p1 = Nf * sit, e1 = fmaf(Nf, sit, -p1);
+                            const float p2 = sIf * st.x, e2 = fmaf(sIf, st.x, -p2);
+                            num = (p1 - p2) + (e1 - e2);
+                        } else {
+                            num = i64_to_f32((long long)((unsigned long long)N * v[i]) -
+                                             (long long)((int)sI) * (long long)st.x);
+                        }
+                        float r = num * (rsI * st.y);
+                        r = fminf(1.0f, fmaxf(-1.0f, r));
+                        __stcs(p.out + oo, r);
                     }
                 }
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -444,15 +483,22 @@ cudaError_t bank_tc_launch(const BankArgs &a, cudaStream_t stream) {
     }
     const int grid = p.ntiles < 2 * g_num_sms[dev] ? p.ntiles : 2 * g_num_sms[dev];
     const size_t smem = (size_t)p.g.smemBytes;
+#define NCC_BANK(M, G1)                                                                          \
+    do {                                                                                         \
+        e = cudaFuncSetAttribute(bank_tc_kernel<M, G1>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                 (int)smem);                                                     \
+        if (e != cudaSuccess) return e;                                                          \
+        bank_tc_kernel<M, G1><<<grid, kThreads, smem, stream>>>(p);                              \
+    } while (0)
+    const bool one = p.g.nG == 1;
     if (a.sumIT) {
-        e = cudaFuncSetAttribute(bank_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        bank_tc_kernel<true><<<grid, kThreads, smem, stream>>>(p);
+        if (one) NCC_BANK(true, true);
+        else NCC_BANK(true, false);
     } else {
-        e = cudaFuncSetAttribute(bank_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        bank_tc_kernel<false><<<grid, kThreads, smem, stream>>>(p);
+        if (one) NCC_BANK(false, true);
+        else NCC_BANK(false, false);
     }
+#undef NCC_BANK
     return cudaGetLastError();
 }
 
