@@ -3,7 +3,8 @@
 One step = the whole path on one 4096x4096 uint8 image and one 16x16 uint8
 template: build both int64 summed-area tables (ncc_sat_build), then the
 numerator and coefficients for all 4081 x 4081 valid shifts (ncc_correlate).
-Prints one JSON line (see the README of the bench contract in the design doc).
+Prints one JSON line: the throughput, per-kernel timings, the roofline of the
+dominant kernel, the CPU oracle baseline, the end-to-end figure and clocks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -49,10 +50,21 @@ def load_peaks() -> dict:
 
 
 # Integer dot-product pipe: dp4a instructions per SM per clock on sm_103a,
-# measured by a throughput microbenchmark (see the design notes); the ALU
+# measured by a throughput microbenchmark (eight independent dp4a chains per
+# thread: 63.9 per SM per clock, the same rate as IMAD); the ALU
 # roofline is this times 152 SMs times the maximum SM clock.
 DP4A_PER_SM_CLK = 64
 N_SMS = 152
+
+# DRAM bytes (read + write) of one launch, from one ncu capture of the bench
+# command (dram__bytes_read.sum + dram__bytes_write.sum; summaries under
+# profiles/).  Keyed by (kernel, workload); an entry is removed whenever its
+# kernel changes, so a stale count is never reported.
+NCU_TRAFFIC_BYTES = {
+    ("sat_build", "ncc_4096_t16"): 228.9e6,
+    ("corr_dp4a", "ncc_4096_t16"): 340.3e6,
+    ("bank_tc", "bank_2048_64x16"): 1073.5e6,
+}
 
 
 def dist_env():
@@ -60,6 +72,23 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of every rank's x (the slowest rank sets the job's time);
+    x itself when running alone."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: int, world_size: int, slowest_ms: float) -> float:
+    """Whole-job throughput under weak scaling: every rank processes the same
+    number of units; the job takes as long as its slowest rank."""
+    return world_size * units_per_rank / (slowest_ms * 1e-3)
 
 
 class ClockSampler:
@@ -236,13 +265,9 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
     t_sat = [ev_a[k].elapsed_time(ev_m[k]) for k in range(args.steps)]
     t_corr = [ev_m[k].elapsed_time(ev_b[k]) for k in range(args.steps)]
     t_step = [a + b for a, b in zip(t_sat, t_corr)]
-    ms_step = statistics.mean(t_step)
-    if dist is not None:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(statistics.mean(t_step), dist, dev)
     coeffs = nT * w.Ox * w.Oy if nT else w.W * w.H
-    value = ws * coeffs / (ms_step * 1e-3)
+    value = job_rate(coeffs, ws, ms_step)
 
     # end to end through the host-buffer entry point (pinned host memory)
     e2e = None
@@ -259,12 +284,8 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
             t0 = time.perf_counter()
             ncc.ncc_match_host(himg, htmp, hout)      # synchronizes the stream
             e2e_t.append(time.perf_counter() - t0)
-        e2e_ms = statistics.mean(e2e_t) * 1e3
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": ws * coeffs / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
+        e2e_ms = max_over_ranks(statistics.mean(e2e_t) * 1e3, dist, dev)
+        e2e = {"value": job_rate(coeffs, ws, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": int(w.image.nbytes + w.templates.nbytes),
                "d2h_bytes_per_step": int(coeffs * 4)}
     if dist is not None:
@@ -278,7 +299,8 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
     sat_ms, corr_ms = statistics.mean(t_sat), statistics.mean(t_corr)
     sat_gbs = SAT_BYTES_PER_PX * w.W * w.H / (sat_ms * 1e-3) / 1e9
     roof_sat = {"kernel": "sat_build", "bound": "hbm", "achieved": sat_gbs, "peak": hbm,
-                "unit": "GB/s", "frac": sat_gbs / hbm, "traffic": None,
+                "unit": "GB/s", "frac": sat_gbs / hbm,
+                "traffic": NCU_TRAFFIC_BYTES.get(("sat_build", w.name)),
                 "peak_source": peaks["source"]}
     rooflines = [roof_sat]
     corr = None
@@ -292,17 +314,19 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
             alu_peak = DP4A_PER_SM_CLK * N_SMS * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
             r2 = {"kernel": "corr_dp4a", "bound": "alu",
                   "achieved": dp4a / (corr_ms * 1e-3) / 1e12, "peak": alu_peak / 1e12,
-                  "unit": "Tdp4a/s", "frac": dp4a / (corr_ms * 1e-3) / alu_peak, "traffic": None}
+                  "unit": "Tdp4a/s", "frac": dp4a / (corr_ms * 1e-3) / alu_peak,
+                  "traffic": NCU_TRAFFIC_BYTES.get(("corr_dp4a", w.name))}
         else:
             # 4 B out per coefficient + S and Q (16 B) + image (1 B) per shift
             corr_bytes = 4 * coeffs + 17 * w.Ox * w.Oy
             tflops = 2.0 * macs / (corr_ms * 1e-3) / 1e12
             peak_tc = float(peaks.get("bf16_tflops", 1900.0))  # f16 runs at the bf16 rate
             r2 = {"kernel": "bank_tc", "bound": "tensor", "achieved": tflops, "peak": peak_tc,
-                  "unit": "TFLOP/s", "frac": tflops / peak_tc, "traffic": None}
+                  "unit": "TFLOP/s", "frac": tflops / peak_tc,
+                  "traffic": NCU_TRAFFIC_BYTES.get(("bank_tc", w.name))}
         corr_gbs = corr_bytes / (corr_ms * 1e-3) / 1e9
         r1 = {"kernel": r2["kernel"], "bound": "hbm", "achieved": corr_gbs, "peak": hbm,
-              "unit": "GB/s", "frac": corr_gbs / hbm, "traffic": None}
+              "unit": "GB/s", "frac": corr_gbs / hbm, "traffic": r2["traffic"]}
         rooflines += [r1, r2]
         corr_roof = max(r1, r2, key=lambda r: r["frac"])
         dominant = roof_sat if sat_ms >= corr_ms else corr_roof
