@@ -115,6 +115,11 @@ int ncc_sat_build_noalloc(const uint8_t *img, int W, int H, int64_t *S,
  *   S, Q device int64 [H][W]: must hold ncc_sat_build(img) output, ordered
  *        before this call (same stream, or an event).
  *   out  device fp32 [Oy][Ox], written completely; must not overlap inputs.
+ * Kernel: the integer dot-product (dp4a) numerator.  A tensor-core
+ * numerator (tcgen05, exact f16 products and fp32 sums) covers hT <= 16,
+ * wT*hT <= 258, wT <= 126, W a multiple of 16 and 16-byte aligned img, S and
+ * Q; it is selected with ncc_debug_set_path(NCC_PATH_TENSOR).  Both produce
+ * the same integer sums; the coefficients agree to fp32 rounding.
  * Returns NCC_OK, NCC_ERR_INVALID_ARG, NCC_ERR_UNSUPPORTED or NCC_ERR_CUDA.
  */
 int ncc_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl,
@@ -184,6 +189,31 @@ int ncc_version(void);
  * operation.  Process-wide; not for concurrent use.
  */
 int ncc_debug_set_fault(int suppress_tile, uint64_t timeout_ns);
+
+/* Kernels a correlate call can launch (ncc_debug_last_path). */
+enum ncc_path_code {
+    NCC_PATH_NONE = 0,
+    NCC_PATH_DP4A = 1,     /* single template, integer dot products         */
+    NCC_PATH_TENSOR = 2,   /* single template, tcgen05 tensor cores          */
+    NCC_PATH_BANK = 3      /* template bank, tcgen05 tensor cores            */
+};
+
+/*
+ * ncc_debug_set_path -- selects the single-template kernel that
+ * ncc_correlate, ncc_correlate_moments and ncc_correlate_bank (for banks the
+ * bank kernel does not take) use.  0 = automatic (dp4a), NCC_PATH_DP4A =
+ * dp4a, NCC_PATH_TENSOR = tensor cores (NCC_ERR_UNSUPPORTED where they do not
+ * apply).  Process-wide; not for concurrent use.
+ * Returns NCC_OK, or NCC_ERR_INVALID_ARG for another value.
+ */
+int ncc_debug_set_path(int path);
+
+/*
+ * ncc_debug_last_path -- the kernel (ncc_path_code) launched by the most
+ * recent successful correlate call of this process; NCC_PATH_NONE before
+ * the first.
+ */
+int ncc_debug_last_path(void);
 
 #ifdef __cplusplus
 }

@@ -358,26 +358,6 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     }
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
 }  // namespace
 
 bool corr_dp4a_supported(int wT, int hT) {
@@ -403,7 +383,7 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
     memset(&tmap, 0, sizeof(tmap));
     bool tma = (a.W % 16 == 0) && ((uintptr_t)a.img % 16 == 0) && p.g.boxW <= kMaxTmaBox &&
                p.g.boxH <= kMaxTmaBox;
-    EncodeTiledFn enc = tma ? encode_fn() : nullptr;
+    EncodeTiledFn enc = tma ? tensor_map_encoder() : nullptr;
     if (enc) {
         const cuuint64_t dims[2] = {(cuuint64_t)a.W, (cuuint64_t)a.H};
         const cuuint64_t strides[1] = {(cuuint64_t)a.W};
@@ -423,7 +403,7 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
     memset(&tmQ, 0, sizeof(tmQ));
     bool tmaEpi = (a.W % 2 == 0) && ((uintptr_t)a.S % 16 == 0) && ((uintptr_t)a.Q % 16 == 0) &&
                   p.g.epiBW <= kMaxTmaBox;
-    if (tmaEpi) enc = encode_fn();
+    if (tmaEpi) enc = tensor_map_encoder();
     if (tmaEpi && enc) {
         const cuuint64_t dims[2] = {(cuuint64_t)a.W, (cuuint64_t)a.H};
         const cuuint64_t strides[1] = {(cuuint64_t)a.W * 8};

@@ -15,9 +15,11 @@ constexpr int kMaxDevices = 64;
 int *g_status_ptr[kMaxDevices] = {};
 std::mutex g_mutex;
 
-// Test hook state (ncc_debug_set_fault).
+// Test hook state (ncc_debug_set_fault, ncc_debug_set_path).
 int g_fault_tile = -1;
 uint64_t g_timeout_ns = 1000000000ull;
+int g_path = 0;
+int g_last_path = NCC_PATH_NONE;
 
 constexpr int kMaxW = 66051;  // 66051 * 255^2 < 2^32: a row's running sum of squares fits uint32
 constexpr long long kMaxN = 66051;  // wT*hT*255^2 < 2^32: SumIT fits uint32
@@ -74,11 +76,19 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
     if (rc != NCC_OK) return rc;
     const size_t Ox = (size_t)(W - wT + 1), Oy = (size_t)(H - hT + 1);
     const size_t plane = Ox * Oy;
+    int path;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        path = g_path;
+    }
     if (nT > 1 && ncc::bank_tc_supported(W, H, wT, hT, nT)) {
         ncc::BankArgs b{img, W, H, tmpl, wT, hT, nT, S, Q, out, sumI, sumI2, sumIT, status};
-        return to_status(ncc::bank_tc_launch(b, stream));
+        rc = to_status(ncc::bank_tc_launch(b, stream));
+        if (rc == NCC_OK) g_last_path = NCC_PATH_BANK;
+        return rc;
     }
-    if (!ncc::corr_dp4a_supported(wT, hT)) return NCC_ERR_UNSUPPORTED;
+    if (path != NCC_PATH_TENSOR && !ncc::corr_dp4a_supported(wT, hT)) return NCC_ERR_UNSUPPORTED;
+    int used = NCC_PATH_NONE;
     for (int t = 0; t < nT; ++t) {
         ncc::CorrArgs a;
         a.img = img; a.W = W; a.H = H;
@@ -91,9 +101,23 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
         a.sumI2 = sumI2;
         a.sumIT = sumIT ? sumIT + (size_t)t * plane : nullptr;
         a.status = status;
-        cudaError_t e = ncc::corr_dp4a_launch(a, stream);
+        cudaError_t e = cudaErrorNotSupported;
+        // Automatic selection takes the dp4a kernel: on the 4096x4096 /
+        // 16x16 workload it measures faster than the tensor-core kernel
+        // (about 200 vs 250 us), whose tiny N = 16 MMAs leave it bound by
+        // pipeline hand-off latency rather than by the tensor pipe.
+        if (path == NCC_PATH_TENSOR && ncc::corr_tc_supported(a)) {
+            e = ncc::corr_tc_launch(a, stream);
+            if (e == cudaSuccess) used = NCC_PATH_TENSOR;
+        }
+        if (e == cudaErrorNotSupported) {
+            if (path == NCC_PATH_TENSOR) return NCC_ERR_UNSUPPORTED;
+            e = ncc::corr_dp4a_launch(a, stream);
+            if (e == cudaSuccess) used = NCC_PATH_DP4A;
+        }
         if (e != cudaSuccess) return to_status(e);
     }
+    g_last_path = used;
     return NCC_OK;
 }
 
@@ -227,6 +251,15 @@ const char *ncc_status_string(int status) {
 }
 
 int ncc_version(void) { return (0 << 16) | 1; }
+
+int ncc_debug_set_path(int path) {
+    if (path != 0 && path != NCC_PATH_DP4A && path != NCC_PATH_TENSOR) return NCC_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_path = path;
+    return NCC_OK;
+}
+
+int ncc_debug_last_path(void) { return g_last_path; }
 
 int ncc_debug_set_fault(int suppress_tile, uint64_t timeout_ns) {
     if (suppress_tile < -1) return NCC_ERR_INVALID_ARG;

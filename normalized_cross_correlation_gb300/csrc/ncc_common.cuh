@@ -3,6 +3,7 @@
 // the bounded look-back wait, and the host launchers' declarations).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -71,6 +72,44 @@ __device__ __forceinline__ unsigned wait_flag(const unsigned *flag, unsigned *ab
 }
 
 // ---------------------------------------------------------------------------
+// Tensor maps for TMA: the driver's cuTensorMapEncodeTiled, looked up once
+// through the runtime (null when the driver does not provide it).
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn tensor_map_encoder() {
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<EncodeTiledFn>(ptr);
+        return nullptr;
+    }();
+    return fn;
+}
+
+// A 2-D row-major tensor map: `elem` bytes per element, dims {W, H}, row
+// stride W*elem bytes, box {boxW, boxH}, no swizzle, zero fill outside.
+inline bool make_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType type, int elem,
+                               const void *base, int W, int H, int boxW, int boxH) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)W, (cuuint64_t)H};
+    const cuuint64_t strides[1] = {(cuuint64_t)W * (cuuint64_t)elem};
+    const cuuint32_t box[2] = {(cuuint32_t)boxW, (cuuint32_t)boxH};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, type, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
 // Host launchers (defined in the kernel translation units).
 // ---------------------------------------------------------------------------
 
@@ -109,6 +148,11 @@ struct CorrArgs {
 };
 bool corr_dp4a_supported(int wT, int hT);
 cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream);
+// The same on the tensor cores (tcgen05; hT <= 16, wT*hT <= 258, wT <= 126,
+// W a multiple of 16, 16-byte aligned img, S and Q).  Returns
+// cudaErrorNotSupported, launching nothing, when the shape does not fit.
+bool corr_tc_supported(const CorrArgs &a);
+cudaError_t corr_tc_launch(const CorrArgs &a, cudaStream_t stream);
 
 // Template-bank correlation on the tensor cores (tcgen05, f16 operands,
 // fp32 accumulation; exact while wT*hT*255^2 < 2^24).

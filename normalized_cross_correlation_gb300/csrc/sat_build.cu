@@ -614,26 +614,6 @@ SatPlan sat_plan(int W, int H) {
     return p;
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &qr) == cudaSuccess &&
-            qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
 // Persistent grid: as many rounds as the resident CTAs need, and the tiles
 // spread evenly over them, so no CTA runs a last round alone.
 int persistent_grid(int ntiles) {
@@ -666,7 +646,7 @@ cudaError_t sat_launch(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
     CUtensorMap tmap;
     memset(&tmap, 0, sizeof(tmap));
     bool tma = (W % 16 == 0) && ((uintptr_t)img % 16 == 0);
-    EncodeTiledFn enc = tma ? encode_fn() : nullptr;
+    EncodeTiledFn enc = tma ? tensor_map_encoder() : nullptr;
     if (enc) {
         const cuuint64_t dims[2] = {(cuuint64_t)W, (cuuint64_t)H};
         const cuuint64_t strides[1] = {(cuuint64_t)W};

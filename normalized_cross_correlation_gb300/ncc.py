@@ -24,7 +24,7 @@ NCC_ERR_NOMEM = -5
 
 EXPORTS = ("ncc_sat_build", "ncc_sat_build_noalloc", "ncc_correlate", "ncc_correlate_bank", "ncc_correlate_moments",
            "ncc_match_host", "ncc_sync_status", "ncc_status_string", "ncc_version",
-           "ncc_debug_set_fault")
+           "ncc_debug_set_fault", "ncc_debug_set_path", "ncc_debug_last_path")
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
             L.ncc_status_string.restype = ctypes.c_char_p
             L.ncc_version.argtypes = []
             L.ncc_debug_set_fault.argtypes = [i, u64]
+            L.ncc_debug_set_path.argtypes = [i]
+            L.ncc_debug_last_path.argtypes = []
             for name in EXPORTS:
                 if name != "ncc_status_string":
                     getattr(L, name).restype = ctypes.c_int
@@ -230,3 +232,16 @@ def ncc_version() -> int:
 
 def ncc_debug_set_fault(suppress_tile: int, timeout_ns: int = 0) -> None:
     _check(lib().ncc_debug_set_fault(int(suppress_tile), int(timeout_ns)), "ncc_debug_set_fault")
+
+
+NCC_PATH_NONE, NCC_PATH_DP4A, NCC_PATH_TENSOR, NCC_PATH_BANK = 0, 1, 2, 3
+
+
+def ncc_debug_set_path(path: int) -> None:
+    """Restricts the single-template kernels (0 = automatic)."""
+    _check(lib().ncc_debug_set_path(int(path)), "ncc_debug_set_path")
+
+
+def ncc_debug_last_path() -> int:
+    """Kernel launched by the most recent successful correlate call."""
+    return int(lib().ncc_debug_last_path())
