@@ -15,28 +15,32 @@
 //   - The tile plus its (wT-1) x (hT-1) halo is one TMA box (cp.async.bulk.
 //     tensor, completion on an mbarrier).  Images whose rows are not a
 //     multiple of 16 bytes, or boxes beyond the TMA limits, use plain loads.
-//   - Four byte-shifted copies of the staged tile (copy d starts d bytes
-//     later) let every lane read 32-bit-aligned groups of four pixels for its
-//     phase d, so the inner loop is two 16-byte shared loads per image row and
-//     template chunk plus, per output row, one broadcast 16-byte template load
-//     and 16 __dp4a -- no byte permutes.  The copies sit 32 bytes (mod 128)
-//     apart so the eight lanes of each shared-load phase hit distinct banks.
+//   - Each lane reads 32 aligned bytes of a tile row (lanes of one qg share
+//     them: conflict-free broadcast loads) and moves them by d bytes with one
+//     byte permute per word, so its four shifts see 32-bit groups of four
+//     pixels; per tile row the cost is 2 shared loads and 7 permutes against
+//     up to 128 __dp4a.
+//   - The numerator loop runs in three phases -- tile rows that meet only
+//     the first output rows, rows that meet all eight, rows that meet only
+//     the last ones -- so no (row, output row) pair is tested at run time
+//     (templates of at least 8 rows; shorter ones take a predicated loop).
 //   - The template is packed into 32-bit words in shared memory, in chunks of
 //     16 pixels, zero-padded to a multiple of 16 (the zero bytes cancel any
 //     pixels read past the window).
 //   - SumIT accumulates in uint32 (exact while wT*hT*255^2 < 2^32).
-//   - Epilogue: the SumIT tile is transposed through shared memory; the CTA
-//     then walks its output rows two at a time (warps 0-3 one row, warps 4-7
-//     the next), one shift per thread.  The four table-row segments a row
-//     needs (S and Q at rows y-1 and y+hT-1, columns x0-2 .. x0+wT+127)
-//     arrive by TMA into a two-stage shared-memory ring; the first stages
-//     are issued before the numerator loop, so their latency hides behind
-//     it.  TMA's zero fill outside the tables implements the four-corner
-//     rule's row -1 / column -1 = 0.  (Tables whose rows are not a multiple
-//     of 16 bytes, or templates wider than 127, read the corners with
-//     coalesced global loads instead.)  num and vI are exact int64; they
-//     become fp32 through two 32-bit halves (the 64-bit convert runs on the
-//     slow fp64 pipe on this part).
+//   - Epilogue: the SumIT tile is transposed through shared memory (over the
+//     dead image tile); the CTA then walks its output rows four at a time,
+//     one shift and two rows per thread.  The table rows a step needs (S and
+//     Q at rows y-1.. and y+hT-1.., columns x0-2 .. x0+wT+127) arrive as four
+//     TMA boxes of four rows each into a two-stage ring -- few, large
+//     requests, since each TMA request costs about a hundred cycles to
+//     issue.  The first stages are issued before the numerator loop.  TMA's
+//     zero fill outside the tables implements the four-corner rule's row -1
+//     / column -1 = 0.  (Tables whose rows are not a multiple of 16 bytes, or
+//     templates wider than 127, read the corners with global loads.)  The
+//     four-corner sums use the low 32 bits of the table entries (exact: the
+//     sums are below 2^32); templates of at most 258 pixels compute the
+//     coefficient in fp32 with exact products, larger ones in exact int64.
 #include "ncc_common.cuh"
 
 #include <cuda.h>
@@ -54,17 +58,16 @@ constexpr int kMaxTmaBox = 256;        // TMA box extent limit per dimension
 constexpr int kMaxSmem = 227 * 1024;   // opt-in shared memory per CTA
 
 constexpr int kEpiStages = 2;          // table-row staging ring depth
-constexpr int kEpiRowsPerStep = 2;     // output rows per epilogue step
-constexpr int kEpiBufs = 4 * kEpiRowsPerStep;  // S/Q x top/bottom x rows
+constexpr int kEpiRowsPerStep = 4;     // output rows per epilogue step (rows per TMA box)
+constexpr int kEpiBufs = 4;            // boxes per stage: S top, S bottom, Q top, Q bottom
 
 struct Geom {
     int nch;         // 16-pixel template chunks
     int boxW;        // staged tile width in bytes = kOutW + 16*nch
     int boxH;        // staged tile height = kOutH + hT - 1
-    int copyStride;  // bytes between shifted copies
-    int tmplOff;     // offset of the packed template
+    int tmplOff;     // offset of the packed template (after the tile / SumIT region)
     int epiBW;       // table-row segment length (int64 elements), even
-    int epiBuf;      // bytes per segment buffer (128-aligned)
+    int epiBuf;      // bytes per box (kEpiRowsPerStep table-row segments, 128-aligned)
     int epiOff;      // offset of the staging ring
     int smemBytes;   // dynamic shared memory (plus 128 bytes of alignment slack)
 };
@@ -74,11 +77,11 @@ Geom make_geom(int wT, int hT) {
     g.nch = (wT + 15) / 16;
     g.boxW = kOutW + 16 * g.nch;
     g.boxH = kOutH + hT - 1;
-    const int copyBytes = g.boxW * g.boxH;
-    g.copyStride = (copyBytes + 127) / 128 * 128 + 32;
-    g.tmplOff = 4 * g.copyStride;  // >= kOutH*kOutW*4: the SumIT transpose reuses the copies
+    const int tileBytes = (g.boxW * g.boxH + 127) / 128 * 128;
+    const int sumBytes = kOutH * kOutW * 4;  // the SumIT transpose reuses the tile's space
+    g.tmplOff = tileBytes > sumBytes ? tileBytes : sumBytes;
     g.epiBW = (kOutW + wT + 2) & ~1;   // columns x0-2 .. x0+wT+127, rounded up to even
-    g.epiBuf = (g.epiBW * 8 + 127) / 128 * 128;
+    g.epiBuf = (kEpiRowsPerStep * g.epiBW * 8 + 127) / 128 * 128;
     g.epiOff = (g.tmplOff + hT * g.nch * 16 + 127) / 128 * 128;
     g.smemBytes = g.epiOff + kEpiStages * kEpiBufs * g.epiBuf + 128;
     return g;
@@ -123,6 +126,18 @@ __device__ __forceinline__ void tma_2d(const CUtensorMap *map, void *dst, int x,
         : "memory");
 }
 
+__device__ __forceinline__ uint32_t mbar_try(unsigned long long *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred P; mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2; selp.u32 %0, 1, 0, P; }"
+        : "=r"(done) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return done;
+}
+
+__device__ __forceinline__ void mbar_arrive(unsigned long long *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Bounded wait on an mbarrier phase; gives up (recording the status) rather
 // than hang if a transfer never lands.
 __device__ __forceinline__ void mbar_wait(unsigned long long *bar, uint32_t parity, int *status) {
@@ -147,6 +162,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     __shared__ __align__(8) unsigned long long s_bar;
     __shared__ __align__(8) unsigned long long s_ebar[kEpiStages];
+    __shared__ __align__(8) unsigned long long s_efree[kEpiStages];
     __shared__ unsigned s_red[kWarps][2];
     __shared__ long long s_sumT, s_vT;
     __shared__ float s_invSqrtVT;
@@ -154,28 +170,30 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     const Geom &g = p.g;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int x0 = blockIdx.x * kOutW, y0 = blockIdx.y * kOutH;
-    const int epiSteps = min(kOutH, p.Oy - y0 + kEpiRowsPerStep - 1) / kEpiRowsPerStep;
+    const int epiSteps = (min(kOutH, p.Oy - y0) + kEpiRowsPerStep - 1) / kEpiRowsPerStep;
     uint8_t *epi = smem + g.epiOff;
     // table-row segments of epilogue step t: rows y0+2t+h, buffers
     // [stage][h][S top, S bottom, Q top, Q bottom]
     auto issue_epi = [&](int t) {
         const int st = t % kEpiStages;
+        const int y = y0 + kEpiRowsPerStep * t;  // first output row of the step
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                     ::"r"(smem_u32(&s_ebar[st])), "r"((uint32_t)(kEpiBufs * g.epiBW * 8))
+                     ::"r"(smem_u32(&s_ebar[st])),
+                       "r"((uint32_t)(kEpiBufs * kEpiRowsPerStep * g.epiBW * 8))
                      : "memory");
-        for (int h = 0; h < kEpiRowsPerStep; ++h) {
-            const int y = y0 + kEpiRowsPerStep * t + h;
-            uint8_t *b = epi + (st * kEpiBufs + 4 * h) * g.epiBuf;
-            tma_2d(&tmS, b, x0 - 2, y - 1, &s_ebar[st]);
-            tma_2d(&tmS, b + g.epiBuf, x0 - 2, y + p.hT - 1, &s_ebar[st]);
-            tma_2d(&tmQ, b + 2 * g.epiBuf, x0 - 2, y - 1, &s_ebar[st]);
-            tma_2d(&tmQ, b + 3 * g.epiBuf, x0 - 2, y + p.hT - 1, &s_ebar[st]);
-        }
+        uint8_t *b = epi + st * kEpiBufs * g.epiBuf;
+        tma_2d(&tmS, b, x0 - 2, y - 1, &s_ebar[st]);                      // rows y-1 ..
+        tma_2d(&tmS, b + g.epiBuf, x0 - 2, y + p.hT - 1, &s_ebar[st]);    // rows y+hT-1 ..
+        tma_2d(&tmQ, b + 2 * g.epiBuf, x0 - 2, y - 1, &s_ebar[st]);
+        tma_2d(&tmQ, b + 3 * g.epiBuf, x0 - 2, y + p.hT - 1, &s_ebar[st]);
     };
 
     if (kTmaEpi && tid == 0) {
-        for (int i = 0; i < kEpiStages; ++i)
+        for (int i = 0; i < kEpiStages; ++i) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_ebar[i])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;"
+                         ::"r"(smem_u32(&s_efree[i])), "r"(kWarps));
+        }
         asm volatile("fence.mbarrier_init.release.cluster;");
         asm volatile("fence.proxy.async.shared::cta;");
         for (int t = 0; t < kEpiStages && t < epiSteps; ++t) issue_epi(t);
@@ -242,52 +260,77 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     if (kTma) mbar_wait(&s_bar, 0, p.status);  // every thread: the tile has landed
     __syncthreads();
 
-    // --- byte-shifted copies 1..3 -----------------------------------------
-    {
-        const uint32_t *c0 = reinterpret_cast<const uint32_t *>(smem);
-        const int words = (g.boxW * g.boxH) / 4;
-        for (int wi = tid; wi < words; wi += kThreads) {
-            // c0[words] is padding: its bytes only meet zero template bytes
-            const uint32_t lo = c0[wi], hi = c0[wi + 1];
-            reinterpret_cast<uint32_t *>(smem + 1 * g.copyStride)[wi] = __byte_perm(lo, hi, 0x4321);
-            reinterpret_cast<uint32_t *>(smem + 2 * g.copyStride)[wi] = __byte_perm(lo, hi, 0x5432);
-            reinterpret_cast<uint32_t *>(smem + 3 * g.copyStride)[wi] = __byte_perm(lo, hi, 0x6543);
-        }
-    }
-    __syncthreads();
-
     // --- numerator: SumIT for 8 rows x 4 shifts per thread -----------------
+    // Lane 4*qg + d reads 32 aligned bytes at 16*qg (+16 per chunk) and
+    // moves them by d bytes with one byte permute per word, so each of its
+    // shifts x0 + 16*qg + 4*k + d sees 32-bit groups of four pixels.
     const int qg = lane >> 2, d = lane & 3;
-    const uint8_t *cp = smem + d * g.copyStride + 16 * qg;
+    const uint32_t sel = 0x3210u + 0x1111u * (uint32_t)d;
+    const uint8_t *cp = smem + 16 * qg;
     uint32_t acc[kRowsPerThread][4];
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i)
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[i][k] = 0u;
 
-    const int rows = kRowsPerThread + p.hT - 1;
     for (int c = 0; c < g.nch; ++c) {
-        const uint8_t *cc = cp + 16 * c;
+        const uint8_t *cc = cp + 16 * c + warp * kRowsPerThread * g.boxW;
         const uint4 *tc = reinterpret_cast<const uint4 *>(tw) + c;  // chunk c of row j at tc[j*nch]
-        for (int r = 0; r < rows; ++r) {
-            const uint8_t *rp = cc + (warp * kRowsPerThread + r) * g.boxW;
+        // the d-shifted words of tile row r of this warp
+        auto row_words = [&](int r, uint32_t (&v)[7]) {
+            const uint8_t *rp = cc + r * g.boxW;
             const uint4 a = *reinterpret_cast<const uint4 *>(rp);
             const uint4 b = *reinterpret_cast<const uint4 *>(rp + 16);
-            const uint32_t v[7] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z};
+            v[0] = __byte_perm(a.x, a.y, sel); v[1] = __byte_perm(a.y, a.z, sel);
+            v[2] = __byte_perm(a.z, a.w, sel); v[3] = __byte_perm(a.w, b.x, sel);
+            v[4] = __byte_perm(b.x, b.y, sel); v[5] = __byte_perm(b.y, b.z, sel);
+            v[6] = __byte_perm(b.z, b.w, sel);
+        };
+        // output row i of the thread += image row (i + j) x template row j
+        auto mac = [&](uint32_t (&a)[4], const uint32_t (&v)[7], const uint4 t) {
 #pragma unroll
-            for (int i = 0; i < kRowsPerThread; ++i) {
-                const int j = r - i;
-                if (j >= 0 && j < p.hT) {
-                    const uint4 t = tc[j * g.nch];
+            for (int k = 0; k < 4; ++k) {
+                uint32_t s = a[k];
+                s = __dp4a(v[k + 0], t.x, s);
+                s = __dp4a(v[k + 1], t.y, s);
+                s = __dp4a(v[k + 2], t.z, s);
+                s = __dp4a(v[k + 3], t.w, s);
+                a[k] = s;
+            }
+        };
+        if (p.hT >= kRowsPerThread) {
+            // tile row r meets output rows i = max(0, r-hT+1) .. min(7, r):
+            // ramp-up rows, full rows and ramp-down rows, without branches
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint32_t s = acc[i][k];
-                        s = __dp4a(v[k + 0], t.x, s);
-                        s = __dp4a(v[k + 1], t.y, s);
-                        s = __dp4a(v[k + 2], t.z, s);
-                        s = __dp4a(v[k + 3], t.w, s);
-                        acc[i][k] = s;
-                    }
+            for (int r = 0; r < kRowsPerThread - 1; ++r) {
+                uint32_t v[7];
+                row_words(r, v);
+#pragma unroll
+                for (int i = 0; i <= r; ++i) mac(acc[i], v, tc[(r - i) * g.nch]);
+            }
+            for (int r = kRowsPerThread - 1; r < p.hT; ++r) {
+                uint32_t v[7];
+                row_words(r, v);
+#pragma unroll
+                for (int i = 0; i < kRowsPerThread; ++i) mac(acc[i], v, tc[(r - i) * g.nch]);
+            }
+#pragma unroll
+            for (int m = 0; m < kRowsPerThread - 1; ++m) {
+                const int r = p.hT + m;
+                uint32_t v[7];
+                row_words(r, v);
+#pragma unroll
+                for (int i = m + 1; i < kRowsPerThread; ++i) mac(acc[i], v, tc[(r - i) * g.nch]);
+            }
+        } else {
+            const int rows = kRowsPerThread + p.hT - 1;
+            for (int r = 0; r < rows; ++r) {
+                uint32_t v[7];
+                row_words(r, v);
+#pragma unroll
+                for (int i = 0; i < kRowsPerThread; ++i) {
+                    const int j = r - i;
+                    if (j >= 0 && j < p.hT) mac(acc[i], v, tc[j * g.nch]);
                 }
             }
         }
@@ -304,56 +347,100 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     __syncthreads();
 
     // --- epilogue: moments from S and Q, coefficient -----------------------
+    // The four-corner sums are below 2^32, so they are formed from the low
+    // 32 bits of the table entries with wrapping arithmetic, exactly.  For
+    // templates of at most 258 pixels every integer involved is below 2^24
+    // and the coefficient is computed in fp32 with exact products (fma
+    // splits); larger templates take exact 64-bit integers.
     const long long N = (long long)p.wT * p.hT;
     const long long sT = s_sumT, vT = s_vT;
     const float invSqrtVT = s_invSqrtVT;
+    const bool smallN = N <= 258;
+    const float Nf = (float)N, sTf = (float)sT;  // exact when smallN
     const int h = warp >> 2, xo = (warp & 3) * 32 + lane, x = x0 + xo;
+    const int segWords = g.epiBW * 2;                          // u32 words per table-row segment
+    const int cl = 2 * (xo + 1), cr = 2 * (xo + p.wT + 1);      // low words of x-1, x+wT-1
     for (int t = 0; t < epiSteps; ++t) {
-        const int row = kEpiRowsPerStep * t + h, y = y0 + row;
-        long long sI = 0, sI2 = 0;
+        const int st = t % kEpiStages;
+        const uint32_t par = (uint32_t)((t / kEpiStages) & 1);
+        // this thread's output rows of the step: h and h + 2
+        uint32_t sIv[2] = {0, 0}, sI2v[2] = {0, 0};
         if (kTmaEpi) {
-            mbar_wait(&s_ebar[t % kEpiStages], (uint32_t)((t / kEpiStages) & 1), p.status);
-            const long long *b = reinterpret_cast<const long long *>(
-                epi + ((t % kEpiStages) * kEpiBufs + 4 * h) * g.epiBuf);
-            const int stride = g.epiBuf / 8;
-            const int cl = xo + 1, cr = xo + p.wT + 1;  // columns x-1 and x+wT-1 from x0-2
-            sI = b[stride + cr] - b[cr] - b[stride + cl] + b[cl];
-            sI2 = b[3 * stride + cr] - b[2 * stride + cr] - b[3 * stride + cl] + b[2 * stride + cl];
-        } else if (y < p.Oy && x < p.Ox) {
+            // one lane polls the stage's barrier for the warp
+            uint32_t done = 0;
+            if (lane == 0) done = mbar_try(&s_ebar[st], par);
+            if (!__shfl_sync(0xffffffffu, done, 0)) mbar_wait(&s_ebar[st], par, p.status);
+            const uint32_t *b = reinterpret_cast<const uint32_t *>(epi + st * kEpiBufs * g.epiBuf);
+            const int box = g.epiBuf / 4;                          // u32 words per box
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int o = (h + 2 * q) * segWords;
+                const uint32_t *St = b + o, *Sb = b + box + o, *Qt = b + 2 * box + o, *Qb = b + 3 * box + o;
+                sIv[q] = Sb[cr] - St[cr] - Sb[cl] + St[cl];
+                sI2v[q] = Qb[cr] - Qt[cr] - Qb[cl] + Qt[cl];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_efree[st]);           // this warp is done with the stage
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+        const int row = kEpiRowsPerStep * t + h + 2 * q, y = y0 + row;
+        uint32_t sI = sIv[q], sI2 = sI2v[q];
+        if (!kTmaEpi && y < p.Oy && x < p.Ox) {
             const size_t W = (size_t)p.W;
             const long long *St = p.S + (size_t)(y - 1) * W, *Sb = p.S + (size_t)(y + p.hT - 1) * W;
             const long long *Qt = p.Q + (size_t)(y - 1) * W, *Qb = p.Q + (size_t)(y + p.hT - 1) * W;
             const int xl = x - 1, xr = x + p.wT - 1;
-            sI = __ldg(Sb + xr);
-            sI2 = __ldg(Qb + xr);
-            if (y > 0) { sI -= __ldg(St + xr); sI2 -= __ldg(Qt + xr); }
-            if (x > 0) { sI -= __ldg(Sb + xl); sI2 -= __ldg(Qb + xl); }
-            if (x > 0 && y > 0) { sI += __ldg(St + xl); sI2 += __ldg(Qt + xl); }
+            sI = (uint32_t)__ldg(Sb + xr);
+            sI2 = (uint32_t)__ldg(Qb + xr);
+            if (y > 0) { sI -= (uint32_t)__ldg(St + xr); sI2 -= (uint32_t)__ldg(Qt + xr); }
+            if (x > 0) { sI -= (uint32_t)__ldg(Sb + xl); sI2 -= (uint32_t)__ldg(Qb + xl); }
+            if (x > 0 && y > 0) { sI += (uint32_t)__ldg(St + xl); sI2 += (uint32_t)__ldg(Qt + xl); }
         }
         if (y < p.Oy && x < p.Ox) {
             const unsigned sumIT = sIT[row * kOutW + xo];
             const size_t o = (size_t)y * p.Ox + x;
             if (kMoments) {
-                p.sumI[o] = sI;
-                p.sumI2[o] = sI2;
+                p.sumI[o] = (long long)sI;
+                p.sumI2[o] = (long long)sI2;
                 p.sumIT[o] = (long long)sumIT;
             } else {
-                // |SumI| < 2^25 and SumT < 2^25; SumI2 < 2^32
-                const long long num = (long long)((unsigned long long)N * sumIT) -
-                                      (long long)((int)sI) * (long long)((int)sT);
-                const long long vI = (long long)((unsigned long long)N * (unsigned)sI2) -
-                                     (long long)((int)sI) * (long long)((int)sI);
+                float num, vIf;
+                bool vIpos;
+                if (smallN) {
+                    // exact N*SumIT - SumI*SumT and N*SumI2 - SumI^2 up to their
+                    // final roundings: both products split exactly by fma, the
+                    // high parts cancel exactly when they are close
+                    const float sit = (float)sumIT, sIf = (float)sI, sI2f = (float)sI2;
+                    const float p1 = Nf * sit, e1 = fmaf(Nf, sit, -p1);
+                    const float p2 = sIf * sTf, e2 = fmaf(sIf, sTf, -p2);
+                    num = (p1 - p2) + (e1 - e2);
+                    const float q1 = Nf * sI2f, f1 = fmaf(Nf, sI2f, -q1);
+                    const float q2 = sIf * sIf, f2 = fmaf(sIf, sIf, -q2);
+                    vIf = (q1 - q2) + (f1 - f2);
+                    vIpos = vIf > 0.f;
+                } else {
+                    // SumI < 2^25 and SumT < 2^25; SumI2 < 2^32
+                    const long long numi = (long long)((unsigned long long)N * sumIT) -
+                                           (long long)sI * (long long)sT;
+                    const long long vI = (long long)((unsigned long long)N * sI2) -
+                                         (long long)sI * (long long)sI;
+                    num = i64_to_f32(numi);
+                    vIpos = vI > 0;
+                    vIf = vIpos ? u64_to_f32((unsigned long long)vI) : 1.f;
+                }
                 float r = 0.0f;
-                if (vI > 0 && vT > 0) {
-                    r = i64_to_f32(num) * rsqrtf(u64_to_f32((unsigned long long)vI)) * invSqrtVT;
+                if (vIpos && vT > 0) {
+                    r = num * rsqrtf(vIf) * invSqrtVT;
                     r = fminf(1.0f, fmaxf(-1.0f, r));
                 }
                 __stcs(p.out + o, r);
             }
         }
-        if (kTmaEpi) {
-            __syncthreads();  // stage (t % kEpiStages) is free again
-            if (tid == 0 && t + kEpiStages < epiSteps) issue_epi(t + kEpiStages);
+        }
+        if (kTmaEpi && tid == 0 && t + kEpiStages < epiSteps) {
+            mbar_wait(&s_efree[st], par, p.status);              // all warps released the stage
+            issue_epi(t + kEpiStages);
         }
     }
 }
@@ -407,7 +494,7 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
     if (tmaEpi && enc) {
         const cuuint64_t dims[2] = {(cuuint64_t)a.W, (cuuint64_t)a.H};
         const cuuint64_t strides[1] = {(cuuint64_t)a.W * 8};
-        const cuuint32_t box[2] = {(cuuint32_t)p.g.epiBW, 1};
+        const cuuint32_t box[2] = {(cuuint32_t)p.g.epiBW, (cuuint32_t)kEpiRowsPerStep};
         const cuuint32_t estr[2] = {1, 1};
         CUresult r1 = enc(&tmS, CU_TENSOR_MAP_DATA_TYPE_INT64, 2, const_cast<int64_t *>(a.S), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
