@@ -169,17 +169,35 @@ __device__ __forceinline__ void mbar_wait(unsigned long long *b, uint32_t parity
     }
 }
 
-__device__ __forceinline__ void tc_commit(unsigned long long *b) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 ::"r"(saddr(b)) : "memory");
+// The same for a whole warp: one lane polls, the answer is shuffled to the
+// others (one barrier access instead of 32; the warp's control flow stays
+// uniform).
+__device__ __forceinline__ void mbar_wait_warp(unsigned long long *b, uint32_t parity, int *abort,
+                                               int *status) {
+    uint32_t done = 0;
+    if ((threadIdx.x & 31u) == 0)
+        asm volatile(
+            "{ .reg .pred P; mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2; selp.u32 %0, 1, 0, P; }"
+            : "=r"(done) : "r"(saddr(b)), "r"(parity) : "memory");
+    if (!__shfl_sync(0xffffffffu, done, 0)) mbar_wait(b, parity, abort, status);
 }
 
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t acc) {
-    asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
-                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+// Issue helpers for a warp that runs the MMA loop uniformly: only the lane
+// with `leader` set issues (a predicate, not a branch, so the descriptor
+// arithmetic stays warp-uniform).
+__device__ __forceinline__ void tc_commit_if(unsigned long long *b, bool leader) {
+    asm volatile("{ .reg .pred q; setp.ne.b32 q, %1, 0;\n"
+                 "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }"
+                 ::"r"(saddr(b)), "r"((uint32_t)leader) : "memory");
 }
+
+__device__ __forceinline__ void tc_mma_if(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t acc, bool leader) {
+    asm volatile("{ .reg .pred p, q; setp.ne.b32 p, %4, 0; setp.ne.b32 q, %5, 0;\n"
+                 "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"((uint32_t)leader) : "memory");
+}
+
 
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile(
@@ -249,8 +267,8 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                                  (n < p.nT && v2 > 0) ? __frsqrt_rn(u64_to_f32((unsigned long long)v2)) : 0.f);
         }
         if (tid == 0) {
-            for (int i = 0; i < g.nx; ++i) { mbar_init(&xfull[i], kProducers); mbar_init(&xempty[i], 1); }
-            for (int i = 0; i < g.na; ++i) { mbar_init(&afull[i], 1); mbar_init(&aempty[i], kEpiThreads); }
+            for (int i = 0; i < g.nx; ++i) { mbar_init(&xfull[i], kProducers / 32); mbar_init(&xempty[i], 1); }
+            for (int i = 0; i < g.na; ++i) { mbar_init(&afull[i], 1); mbar_init(&aempty[i], kEpiThreads / 32); }
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             s_abort = 0;
         }
@@ -280,18 +298,31 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
         if (warp >= 1 && warp <= 3) {
             // ---- producers: image rows -> f16 shifted-copy A buffers ----
             const int pt = tid - 32;
+            const bool aligned8 = (p.W % 8 == 0) && ((uintptr_t)p.img % 8 == 0);
             for (int rl = 0; rl < nrows; ++rl) {
                 const uint32_t q = rowSeq + rl, slot = q % g.nx, k = q / g.nx;
-                if (k > 0) mbar_wait(&xempty[slot], (k - 1) & 1, &s_abort, p.status);
+                if (k > 0) mbar_wait_warp(&xempty[slot], (k - 1) & 1, &s_abort, p.status);
                 uint8_t *X = smem + g.offX + slot * g.xBytes;
                 const uint8_t *src = p.img + (size_t)(y0 + rl) * p.W;
                 for (int row = pt; row < g.xBlocks * 8; row += kProducers) {
-                    const int c0 = x0 + 8 * (row >> 3) + (row & 7);  // pixel of element 0
+                    const int xb = x0 + 8 * (row >> 3), sh = row & 7;
+                    const int c0 = xb + sh;  // pixel of element 0
                     uint32_t w0 = 0, w1 = 0;
+                    if (aligned8 && xb + 16 <= p.W) {
+                        // two aligned 8-byte loads, then a funnel shift by sh bytes
+                        const uint2 lo = __ldg(reinterpret_cast<const uint2 *>(src + xb));
+                        const uint2 hi = __ldg(reinterpret_cast<const uint2 *>(src + xb + 8));
+                        const bool up = sh >= 4;
+                        const uint32_t a0 = up ? lo.y : lo.x, a1 = up ? hi.x : lo.y,
+                                       a2 = up ? hi.y : hi.x;
+                        w0 = __funnelshift_r(a0, a1, 8u * (uint32_t)(sh & 3));
+                        w1 = __funnelshift_r(a1, a2, 8u * (uint32_t)(sh & 3));
+                    } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (c0 + e < p.W) w0 |= (uint32_t)__ldg(src + c0 + e) << (8 * e);
-                        if (c0 + 4 + e < p.W) w1 |= (uint32_t)__ldg(src + c0 + 4 + e) << (8 * e);
+                        for (int e = 0; e < 4; ++e) {
+                            if (c0 + e < p.W) w0 |= (uint32_t)__ldg(src + c0 + e) << (8 * e);
+                            if (c0 + 4 + e < p.W) w1 |= (uint32_t)__ldg(src + c0 + 4 + e) << (8 * e);
+                        }
                     }
                     uint4 h;
                     h.x = bytes_to_h2(w0, 0x4140);
@@ -301,13 +332,17 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                     *reinterpret_cast<uint4 *>(X + row * 16) = h;
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive(&xfull[slot]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&xfull[slot]);
             }
         } else if (warp == 0) {
             // ---- MMA issuer ----
             // Descriptors are linear in the shared address (field = addr >> 4),
             // so the loop only adds precomputed steps: no divisions per MMA.
-            if (lane == 0) {
+            // The whole warp runs the loop (warp-uniform descriptors); lane 0
+            // alone issues the MMAs and commits.
+            {
+                const bool leader = lane == 0;
                 const uint64_t adesc0 = smem_desc(saddr(smem + g.offX), 128, 128);
                 const uint64_t bdesc0 = smem_desc(saddr(smem + g.offB), g.nTpad * 16, 128);
                 const uint32_t xStep = (uint32_t)g.xBytes >> 4;                 // next A buffer
@@ -318,10 +353,10 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                 int ready = 0;  // image rows of this tile known to be converted
                 for (int yl = 0; yl < ty; ++yl) {
                     const uint32_t o = outSeq + yl, a = o % g.na, ka = o / g.na;
-                    if (ka > 0) mbar_wait(&aempty[a], (ka - 1) & 1, &s_abort, p.status);
+                    if (ka > 0) mbar_wait_warp(&aempty[a], (ka - 1) & 1, &s_abort, p.status);
                     while (ready < yl + p.hT) {
                         const uint32_t q = rowSeq + ready;
-                        mbar_wait(&xfull[readySlot], (q / g.nx) & 1, &s_abort, p.status);
+                        mbar_wait_warp(&xfull[readySlot], (q / g.nx) & 1, &s_abort, p.status);
                         ++ready;
                         if (++readySlot == (uint32_t)g.nx) readySlot = 0;
                     }
@@ -333,16 +368,16 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                     for (int j = 0; j < p.hT; ++j) {
                         const uint64_t ad = adesc0 + (uint64_t)(s * xStep);
                         for (int c = 0; c < g.nK16; ++c)
-                            tc_mma(d, ad + 16u * c, bd + c * bChunk, idesc,
-                                   (inGroup != 0 || c != 0) ? 1u : 0u);
+                            tc_mma_if(d, ad + 16u * c, bd + c * bChunk, idesc,
+                                      (inGroup != 0 || c != 0) ? 1u : 0u, leader);
                         bd += bRow;
                         if (++s == (uint32_t)g.nx) s = 0;
                         if (++inGroup == g.G) { inGroup = 0; d += g.nTpad; }
                     }
-                    tc_commit(&afull[a]);
-                    tc_commit(&xempty[(slot0 + yl) % g.nx]);  // image row y0+yl is done
+                    tc_commit_if(&afull[a], leader);
+                    tc_commit_if(&xempty[(slot0 + yl) % g.nx], leader);  // image row y0+yl is done
                 }
-                for (int rl = ty; rl < nrows; ++rl) tc_commit(&xempty[(slot0 + rl) % g.nx]);
+                for (int rl = ty; rl < nrows; ++rl) tc_commit_if(&xempty[(slot0 + rl) % g.nx], leader);
             }
             __syncwarp();
         } else {
@@ -377,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                                      (long long)((int)sI) * (long long)((int)sI);
                 const float rsI = vI > 0 ? rsqrtf(u64_to_f32((unsigned long long)vI)) : 0.f;
                 const float sIf = (float)(int)sI;  // < 2^25: exact
-                mbar_wait(&afull[a], ka & 1, &s_abort, p.status);
+                mbar_wait_warp(&afull[a], ka & 1, &s_abort, p.status);
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const size_t obase = (size_t)y * p.Ox + x;
                 if (kMoments && xin && ch == 0) {
@@ -430,7 +465,8 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                     }
                 }
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-                mbar_arrive(&aempty[a]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&aempty[a]);
             }
         }
         rowSeq += nrows;
