@@ -121,15 +121,12 @@ struct SatPlan {
     size_t total_bytes;     // whole workspace
 };
 SatPlan sat_plan(int W, int H);
-// One launch of the builder on a caller-provided workspace.  `epoch` (1..31)
-// tags this call's look-back words; `ticket_base` is the workspace's ticket
-// counter value before the launch; *tickets_used (optional) receives how far
-// the launch advances that counter.
+// One launch of the builder on a caller-provided workspace whose first
+// zero_bytes are zero (a launch leaves them zero again when it ends).
+// `epoch` (1..31) tags this call's look-back words.
 cudaError_t sat_launch(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
-                       void *workspace, const SatPlan &plan, uint32_t epoch,
-                       unsigned long long ticket_base, int *status, uint64_t timeout_ns,
-                       int fault_tile, cudaStream_t stream,
-                       unsigned long long *tickets_used = nullptr);
+                       void *workspace, const SatPlan &plan, uint32_t epoch, int *status,
+                       uint64_t timeout_ns, int fault_tile, cudaStream_t stream);
 // The builder on the library's per-device workspace (allocated on first use).
 cudaError_t sat_build_run(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
                           int *status, uint64_t timeout_ns, int fault_tile,

@@ -4,23 +4,34 @@
 //
 // Design (GB300).  The image is cut into tiles of 128 columns by 128 rows,
 // handed out by an atomic ticket in row-major order to a persistent grid
-// (three CTAs per SM).  Each CTA runs two warp groups over a double-buffered
-// shared-memory stage:
-//   - producer warps 0-3 take a ticket, load the tile's pixels with
-//     one TMA box per tile, issued a tile ahead into a three-slot pixel
-//     ring (plain loads when rows are not 16-byte multiples), scan each
-//     row segment (four columns per lane, 32 rows per warp) in uint32 with
-//     warp shuffles (a row's running
-//     sum of squares is at most W*255^2 < 2^32 for W <= 66051), then get
-//     each row's carry from the tiles to its left and each column's carry
-//     from the tiles above by decoupled look-backs -- the section's
-//     three-state protocol (empty / aggregate published / inclusive prefix
-//     published) -- and leave pixels, row carries and each writer group's
-//     starting column sums in the stage;
-//   - writer warps 4-7 rebuild the rows from the stage and stream S and Q
-//     out as int64 with 16-byte streaming stores.
+// (three CTAs on every SM).  Each CTA runs two warp groups over a
+// double-buffered shared-memory stage:
+//   - producer warps 0-3 take a ticket, load the tile's pixels with one TMA
+//     box per tile, issued a tile ahead into a three-slot pixel ring (plain
+//     loads when rows are not 16-byte multiples).  Thread pt owns row pt and
+//     column pt: it sums its row with byte dot products (in uint32: a row's
+//     running sum of squares is at most W*255^2 < 2^32 for W <= 66051) and
+//     publishes it at once, then forms the column sums of the warp-local
+//     row prefixes while its first look-back loads are in flight, and gets
+//     the row's carry from the tiles to its left and the column's carry from
+//     the tiles above by decoupled look-backs -- the section's three-state
+//     protocol (empty / aggregate published / inclusive prefix published).
+//     The stage receives the row carries and each writer group's starting
+//     column sums;
+//   - writer warps 4-7 rebuild the rows from the pixels, four rows at a
+//     time so that their warp scans overlap, and stream S and Q out as
+//     int64 with 32-byte stores.
 // The look-back latency of one tile thus overlaps the writes of the
 // previous one inside every CTA.
+//
+// Sharing the tiles.  One SM stores at most about 28 bytes per clock,
+// whatever its warps or store instructions, and the tables are 16 of the
+// 17 bytes per pixel, so an SM that writes one tile more than the others
+// ends one tile's store time later.  The ticket rule therefore evens out
+// tiles per SM, not per CTA: a CTA draws only while its SM holds fewer than
+// ceil(tiles / SMs) tiles and no more than its share of the tiles drawn so
+// far; otherwise it naps (at most kShareWaitNs) until the tiles run out.
+// The last CTA to finish returns the ticket and the SM counters to zero.
 //
 // Look-back words.  Every published value is one 64-bit word holding
 // {epoch:5, state:2, value:57}, written and read with single-copy-atomic
@@ -28,8 +39,12 @@
 // publication needs no separate flag or fence.  Row words pack the row's
 // sum of I (25 bits) and of I^2 (32 bits) -- both fit for W <= 66051 and
 // their sums never carry across fields.  Column words carry S (< 2^39) or
-// Q (< 2^47) of one column, one word each.  A waiting thread reads up to
-// kWindow predecessors with independent loads per round.  The epoch tag
+// Q (< 2^47) of one column, one word each.  A waiting thread reads a
+// window of predecessors with independent loads per round, and a producer
+// thread keeps its row's window and its column's windows in flight together:
+// the column look-back reads only the tiles above, so it runs during the row
+// look-back, and only this tile's own column publication waits for the row
+// carries (its column sums include them).  The epoch tag
 // lets the workspace be reused without clearing it: a word from an earlier
 // call reads as empty.
 //
@@ -54,9 +69,14 @@ constexpr int kThreads = 2 * kProducers;
 constexpr int kRowsPerWarp = 32;
 constexpr int kTileH = kGroups * kRowsPerWarp;  // 128
 constexpr int kCtasPerSm = 3;
+constexpr int kMaxSmIds = 1024;       // per-SM tile counters (indexed by %smid)
+constexpr uint64_t kShareWaitNs = 40000;  // longest nap of a CTA whose SM is ahead of its share
+constexpr int kShareQ = 4;            // an SM may run ahead of its share by kShareQ/4 tile
 constexpr int kStageDone = -1, kStageAbort = -2;
 constexpr int kColWords = 2 * kTileW;          // S and Q word per column
-constexpr int kWindow = 8;            // predecessors read per look-back round
+constexpr int kRowWindow = 8;         // row predecessors read per look-back round
+constexpr int kColWindowEarly = 4;    // column predecessors read alongside the row look-back
+constexpr int kColWindow = 8;         // column predecessors read per round afterwards
 
 constexpr int kEpochShift = 59, kStateShift = 57;
 constexpr uint64_t kValueMask = (1ull << kStateShift) - 1;
@@ -64,8 +84,10 @@ constexpr int kRowQShift = 25;        // row word: I in bits 0..24, I^2 in 25..5
 constexpr uint32_t kMaxEpoch = 31;
 
 struct SatWs {
-    unsigned long long *ticket;  // tile dispenser: ticket - ticket_base = tile index
+    unsigned long long *ticket;  // tile dispenser (ticket = tile index); 0 between launches
     unsigned *abort;             // holds the epoch of a call whose wait ran out
+    unsigned *done;              // CTAs finished; the last one resets the counters
+    unsigned *smTiles;           // [kMaxSmIds] tiles drawn by the CTAs of each SM
     uint64_t *row;               // [ntiles][kTileH] row words
     uint64_t *col;               // [ntiles][kColWords] column words (S part, then Q part)
 };
@@ -89,25 +111,61 @@ __device__ __forceinline__ uint32_t word_state(uint64_t w, uint32_t epoch) {
                                                     : FLAG_EMPTY;
 }
 
-// Inclusive scan of one 128-pixel row segment held as four bytes per lane:
-// p[c] / s[c] = sum of pixels / of squared pixels from the warp's first
-// column up to this lane's column c (uint32).  Lane 31's p[3], s[3] are the
-// segment's totals.
-__device__ __forceinline__ void row_scan(uint32_t px, int lane, uint32_t (&p)[4],
-                                         uint32_t (&s)[4]) {
-    const uint32_t b0 = px & 255u, b1 = (px >> 8) & 255u, b2 = (px >> 16) & 255u, b3 = px >> 24;
-    p[0] = b0; p[1] = p[0] + b1; p[2] = p[1] + b2; p[3] = p[2] + b3;
-    s[0] = b0 * b0; s[1] = s[0] + b1 * b1; s[2] = s[1] + b2 * b2; s[3] = s[2] + b3 * b3;
-    uint32_t sI = p[3], sQ = s[3];
+// Inclusive scans of kScanRows 128-pixel row segments, four bytes per lane:
+// p[j][c] / s[j][c] = sum of pixels / of squared pixels of row j from the
+// warp's first column up to this lane's column c (uint32).  The lane-local
+// prefixes come from byte dot products; the sums over the lanes to the left
+// come from one shuffle scan in which two rows' pixel sums share a word
+// (each at most 128 * 255 < 2^16), so the rows' chains run side by side.
+constexpr int kScanRows = 4;
+__device__ __forceinline__ void row_scan_rows(const uint32_t (&px)[kScanRows], int lane,
+                                              uint32_t (&p)[kScanRows][4],
+                                              uint32_t (&s)[kScanRows][4]) {
+    uint32_t tI[kScanRows / 2], tQ[kScanRows];
+#pragma unroll
+    for (int j = 0; j < kScanRows; ++j) {
+        const uint32_t v = px[j];
+        p[j][0] = v & 0xffu;
+        p[j][1] = __dp4a(v, 0x00000101u, 0u);
+        p[j][2] = __dp4a(v, 0x00010101u, 0u);
+        p[j][3] = __dp4a(v, 0x01010101u, 0u);
+        s[j][0] = __dp4a(v, v & 0x000000ffu, 0u);
+        s[j][1] = __dp4a(v, v & 0x0000ffffu, 0u);
+        s[j][2] = __dp4a(v, v & 0x00ffffffu, 0u);
+        s[j][3] = __dp4a(v, v, 0u);
+        tQ[j] = s[j][3];
+    }
+#pragma unroll
+    for (int h = 0; h < kScanRows / 2; ++h) tI[h] = p[2 * h][3] | (p[2 * h + 1][3] << 16);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t tI = __shfl_up_sync(0xffffffffu, sI, o);
-        const uint32_t tQ = __shfl_up_sync(0xffffffffu, sQ, o);
-        if (lane >= o) { sI += tI; sQ += tQ; }
-    }
-    const uint32_t eI = sI - p[3], eQ = sQ - s[3];
+        uint32_t uI[kScanRows / 2], uQ[kScanRows];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) { p[c] += eI; s[c] += eQ; }
+        for (int h = 0; h < kScanRows / 2; ++h) uI[h] = __shfl_up_sync(0xffffffffu, tI[h], o);
+#pragma unroll
+        for (int j = 0; j < kScanRows; ++j) uQ[j] = __shfl_up_sync(0xffffffffu, tQ[j], o);
+        if (lane >= o) {
+#pragma unroll
+            for (int h = 0; h < kScanRows / 2; ++h) tI[h] += uI[h];
+#pragma unroll
+            for (int j = 0; j < kScanRows; ++j) tQ[j] += uQ[j];
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < kScanRows / 2; ++h) {
+        // exclusive = inclusive - own; neither half borrows (each half's
+        // inclusive sum includes its own term)
+        const uint32_t e = tI[h] - (p[2 * h][3] | (p[2 * h + 1][3] << 16));
+        const uint32_t e0 = e & 0xffffu, e1 = e >> 16;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) { p[2 * h][c] += e0; p[2 * h + 1][c] += e1; }
+    }
+#pragma unroll
+    for (int j = 0; j < kScanRows; ++j) {
+        const uint32_t e = tQ[j] - s[j][3];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s[j][c] += e;
+    }
 }
 
 struct WaitCtx {
@@ -117,112 +175,81 @@ struct WaitCtx {
     uint64_t t0, timeout_ns;
 };
 
-// Decoupled look-back of one element over `count` predecessors whose words
-// sit at words[(first - i*step) * tstride], i = 0..count-1 (nearest first).
-// Adds the values of consecutive published predecessors up to and including
-// the nearest inclusive prefix into `acc`.  Returns false when a wait ran
-// out or another CTA of the call aborted.
-__device__ __forceinline__ bool look_back(const uint64_t *words, size_t tstride, int first,
-                                          int step, int count, uint64_t &acc,
-                                          const WaitCtx &cx) {
-    int i0 = 0;
-    unsigned backoff = 32, polls = 0;
-    while (i0 < count) {
-        uint64_t w[kWindow];
-#pragma unroll
-        for (int i = 0; i < kWindow; ++i)
-            w[i] = (i0 + i < count)
-                       ? ld_relaxed_u64(words + (size_t)(first - (i0 + i) * step) * tstride)
-                       : 0ull;
-        int used = 0;
-        bool done = false;
-#pragma unroll
-        for (int i = 0; i < kWindow; ++i) {
-            if (used == i && !done && i0 + i < count) {
-                const uint32_t st = word_state(w[i], cx.epoch);
-                if (st != FLAG_EMPTY) {
-                    acc += w[i] & kValueMask;
-                    used = i + 1;
-                    done = (st == FLAG_PREFIX);
-                }
-            }
-        }
-        if (done) return true;
-        if (used == 0) {
-            // the nearest unconsumed predecessor has not published yet
-            __nanosleep(backoff);
-            if (backoff < 256) backoff <<= 1;
-            if ((++polls & 7u) == 0u) {
-                if (ld_relaxed_gpu(cx.abort) == cx.epoch) return false;
-                if (global_timer_ns() - cx.t0 > cx.timeout_ns || polls > (1u << 26)) {
-                    atomicExch(cx.abort, cx.epoch);
-                    record_status(cx.status, NCC_ERR_TIMEOUT);
-                    return false;
-                }
-            }
-            continue;
-        }
-        i0 += used;
-    }
-    return true;
+// One decoupled look-back in progress: the predecessors' words of one
+// element sit at p0 + i*delta, i = 0..count-1 (nearest first).  `acc`
+// gathers the values of consecutive published predecessors; the chain is
+// done at the first inclusive prefix or after the last predecessor.  Loads
+// and examination are separate steps so that a thread can keep several
+// chains' windows in flight in one round trip.
+struct Chain {
+    const uint64_t *p0;
+    long long delta;
+    int count, next;
+    uint64_t acc;
+    bool done;
+};
+
+__device__ __forceinline__ Chain make_chain(const uint64_t *p0, long long delta, int count) {
+    Chain c;
+    c.p0 = p0;
+    c.delta = delta;
+    c.count = count;
+    c.next = 0;
+    c.acc = 0;
+    c.done = count <= 0;
+    return c;
 }
 
-// The same look-back for two independent chains at once (the S and Q words
-// of one column): both windows are loaded before either is examined, so the
-// two chains share each round trip.
-__device__ __forceinline__ bool look_back2(const uint64_t *w0s, const uint64_t *w1s, size_t tstride,
-                                           int first, int step, int count, uint64_t &acc0,
-                                           uint64_t &acc1, const WaitCtx &cx) {
-    int i0[2] = {0, 0};
-    bool done[2] = {count == 0, count == 0};
-    uint64_t acc[2] = {0, 0};
-    unsigned backoff = 32, polls = 0;
-    while (!done[0] || !done[1]) {
-        uint64_t w[2][kWindow];
+template <int N>
+__device__ __forceinline__ void chain_load(const Chain &c, uint64_t (&w)[N]) {
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
+    for (int i = 0; i < N; ++i)
+        w[i] = (!c.done && c.next + i < c.count) ? ld_relaxed_u64(c.p0 + (long long)(c.next + i) * c.delta)
+                                                 : 0ull;
+}
+
+// Consumes the loaded window up to the first empty word; returns whether
+// anything was consumed.
+template <int N>
+__device__ __forceinline__ bool chain_take(Chain &c, const uint64_t (&w)[N], uint32_t epoch) {
+    if (c.done) return false;
+    int used = 0;
+    bool prefix = false;
 #pragma unroll
-            for (int i = 0; i < kWindow; ++i)
-                w[q][i] = (!done[q] && i0[q] + i < count)
-                              ? ld_relaxed_u64((q ? w1s : w0s) + (size_t)(first - (i0[q] + i) * step) * tstride)
-                              : 0ull;
-        bool stalled = true;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            if (done[q]) continue;
-            int used = 0;
-#pragma unroll
-            for (int i = 0; i < kWindow; ++i) {
-                if (used == i && !done[q] && i0[q] + i < count) {
-                    const uint32_t st = word_state(w[q][i], cx.epoch);
-                    if (st != FLAG_EMPTY) {
-                        acc[q] += w[q][i] & kValueMask;
-                        used = i + 1;
-                        done[q] = (st == FLAG_PREFIX);
-                    }
-                }
-            }
-            i0[q] += used;
-            if (i0[q] >= count) done[q] = true;
-            if (used) stalled = false;
-        }
-        if (stalled && (!done[0] || !done[1])) {
-            __nanosleep(backoff);
-            if (backoff < 256) backoff <<= 1;
-            if ((++polls & 7u) == 0u) {
-                if (ld_relaxed_gpu(cx.abort) == cx.epoch) return false;
-                if (global_timer_ns() - cx.t0 > cx.timeout_ns || polls > (1u << 26)) {
-                    atomicExch(cx.abort, cx.epoch);
-                    record_status(cx.status, NCC_ERR_TIMEOUT);
-                    return false;
-                }
+    for (int i = 0; i < N; ++i) {
+        if (used == i && !prefix && c.next + i < c.count) {
+            const uint32_t st = word_state(w[i], epoch);
+            if (st != FLAG_EMPTY) {
+                c.acc += w[i] & kValueMask;
+                used = i + 1;
+                prefix = (st == FLAG_PREFIX);
             }
         }
     }
-    acc0 += acc[0];
-    acc1 += acc[1];
-    return true;
+    c.next += used;
+    if (prefix || c.next >= c.count) c.done = true;
+    return used > 0;
 }
+
+// Back-off between polls that found nothing new.  Returns false when the
+// wait ran out (recorded as NCC_ERR_TIMEOUT, and the call's abort word
+// raised) or another CTA of the call aborted.
+struct Backoff {
+    unsigned ns = 32, polls = 0;
+    __device__ __forceinline__ bool wait(const WaitCtx &cx) {
+        __nanosleep(ns);
+        if (ns < 256) ns <<= 1;
+        if ((++polls & 7u) == 0u) {
+            if (ld_relaxed_gpu(cx.abort) == cx.epoch) return false;
+            if (global_timer_ns() - cx.t0 > cx.timeout_ns || polls > (1u << 26)) {
+                atomicExch(cx.abort, cx.epoch);
+                record_status(cx.status, NCC_ERR_TIMEOUT);
+                return false;
+            }
+        }
+        return true;
+    }
+};
 
 // 32 contiguous bytes (four int64) in one 256-bit store: a lane fills one
 // whole L2 sector, a warp 1 KB.
@@ -244,9 +271,11 @@ __device__ __forceinline__ void named_bar_arrive(int id, int n) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// After a failed wait the CTA stops, but it still draws tickets until one
-// lies past the last tile, so that every launch advances the ticket counter
-// by exactly ntiles + gridDim.x (the host's next ticket base relies on it).
+__device__ __forceinline__ unsigned sm_id() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
+}
 
 // One double-buffered hand-off from the producer warps to the writer warps.
 struct Stage {
@@ -270,26 +299,47 @@ template <bool kTma, bool kAligned4, int kStore>
 __global__ void __launch_bounds__(kThreads, 3)
 sat_build_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__restrict__ img,
                  int W, int H, long long *__restrict__ S, long long *__restrict__ Q, SatWs ws,
-                 int ntx, int ntiles, uint32_t epoch, unsigned long long ticket_base,
+                 int ntx, int ntiles, uint32_t epoch, int nsm, int smCap, int shareQ,
                  int *status, uint64_t timeout_ns, int fault_tile) {
     extern __shared__ __align__(128) uint8_t s_dyn[];
     uint8_t (*s_pix)[kTileH][kTileW] = reinterpret_cast<uint8_t (*)[kTileH][kTileW]>(
         (reinterpret_cast<uintptr_t>(s_dyn) + 127) & ~uintptr_t(127));
     __shared__ __align__(16) Stage st[2];
-    __shared__ uint2 s_rowTot[kTileH];                          // tile row sums
-    __shared__ uint2 s_rowCarry[kTileH];
     __shared__ __align__(16) uint2 s_colPart[kGroups][kTileW];  // per-warp column sums of warp-local prefixes
     __shared__ long long s_warpCarry[kGroups][2];               // per-warp sums of the row carries
     __shared__ __align__(8) unsigned long long s_pbar[kPixSlots];
     __shared__ unsigned s_tile, s_next;
-    __shared__ int s_fail;
+    __shared__ int s_fail, s_last;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (warp < kGroups) {
         // ================= producer warps: tiles, scans, look-backs =================
         const int pt = tid;  // 0..127
+        // Next tile.  One SM's store rate is what bounds the build, so the
+        // tiles are shared out evenly over the SMs rather than the CTAs: a
+        // CTA draws only while its SM holds fewer than smCap tiles and no
+        // more than its share of the tiles drawn so far (plus shareQ/4 of a
+        // tile); otherwise it naps, so that SMs behind draw first, until the
+        // tiles run out.  The naps end after kShareWaitNs at the latest:
+        // correctness never depends on other CTAs being resident.
         auto grab = [&]() -> unsigned {
-            return (unsigned)(atomicAdd(ws.ticket, 1ull) - ticket_base);
+            const unsigned smSlot = sm_id() % kMaxSmIds;
+            const uint64_t w0 = global_timer_ns();
+            for (;;) {
+                // reserve the SM's next slot first, so that CTAs of one SM
+                // deciding at once see each other; hand it back on a nap
+                const unsigned c = atomicAdd(ws.smTiles + smSlot, 1u);
+                const unsigned long long t = ld_relaxed_u64(reinterpret_cast<const uint64_t *>(ws.ticket));
+                if (t >= (unsigned long long)ntiles || c < (unsigned)kCtasPerSm ||
+                    (c < (unsigned)smCap &&
+                     4ull * c * (unsigned)nsm <= 4ull * t + (unsigned long long)shareQ * (unsigned)nsm) ||
+                    global_timer_ns() - w0 > kShareWaitNs)
+                    break;
+                atomicSub(ws.smTiles + smSlot, 1u);
+                __nanosleep(256);
+            }
+            const unsigned long long t = atomicAdd(ws.ticket, 1ull);
+            return t < (unsigned long long)ntiles ? (unsigned)t : (unsigned)ntiles;
         };
         // pixels of `tile` into ring slot `slot`: one TMA box (completion on
         // s_pbar[slot]); tiles past the image edge read zeros
@@ -370,87 +420,101 @@ sat_build_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__rest
                 }
                 __syncwarp();
             }
-            // 2. row totals and column sums of the warp-local row prefixes,
-            //    without per-row scans: the prefix at (row k, lane L, column c)
-            //    is (sum of row k's lanes < L) + (lane L's own pixels up to c),
-            //    so its sum over the 32 rows is one exclusive lane scan of the
-            //    lanes' 32-row totals plus the lane-local prefix sums.
-            uint32_t cI[4] = {0, 0, 0, 0}, cQ[4] = {0, 0, 0, 0};
-            uint32_t sumI = 0, sumQ = 0;  // this lane's total over the warp's rows
+            // 2. this thread's row total (row pt, read with the word order
+            //    rotated by the lane so that a warp's 32 rows hit 32 banks),
+            //    published at once as the row's aggregate
+            const uint8_t *myRow = &s_pix[ps][pt][0];
+            uint32_t rowI = 0, rowQ = 0;
 #pragma unroll 8
-            for (int k = 0; k < kRowsPerWarp; ++k) {
-                const uint32_t v =
-                    *reinterpret_cast<const uint32_t *>(&s_pix[ps][warp * kRowsPerWarp + k][4 * lane]);
-                const uint32_t b0 = v & 255u, b1 = (v >> 8) & 255u, b2 = (v >> 16) & 255u, b3 = v >> 24;
-                const uint32_t i1 = b0 + b1, i2 = i1 + b2, i3 = i2 + b3;
-                const uint32_t q0 = b0 * b0, q1 = q0 + b1 * b1, q2 = q1 + b2 * b2, q3 = q2 + b3 * b3;
-                cI[0] += b0; cI[1] += i1; cI[2] += i2; cI[3] += i3;
-                cQ[0] += q0; cQ[1] += q1; cQ[2] += q2; cQ[3] += q3;
-                sumI += i3;
-                sumQ += q3;
-                const uint32_t totI = __reduce_add_sync(0xffffffffu, i3);
-                const uint32_t totQ = __reduce_add_sync(0xffffffffu, q3);
-                if (lane == 0) s_rowTot[warp * kRowsPerWarp + k] = make_uint2(totI, totQ);
+            for (int j = 0; j < kTileW / 4; ++j) {
+                const uint32_t v = *reinterpret_cast<const uint32_t *>(myRow + 4 * ((j + lane) & 31));
+                rowI = __dp4a(v, 0x01010101u, rowI);
+                rowQ = __dp4a(v, v, rowQ);
             }
+            const uint64_t rowV = (uint64_t)rowI | ((uint64_t)rowQ << kRowQShift);
+            uint64_t *rowMine = ws.row + (size_t)tile * kTileH + pt;
+            if (publish)
+                st_relaxed_u64(rowMine, make_word(epoch, tx == 0 ? FLAG_PREFIX : FLAG_AGGREGATE, rowV));
+
+            // 3. row carry by look-back to the left.  The column look-back
+            //    (thread pt also owns column pt) reads only the tiles above,
+            //    so its windows ride along in the same round trips; it
+            //    finishes in step 5, once this tile's column sums are known.
+            //    The first windows are in flight while the column sums of
+            //    the warp-local row prefixes are formed.
+            Chain row = make_chain(rowMine - kTileH, -(long long)kTileH, tx);
+            Chain colS = make_chain(ws.col + (long long)((int)tile - ntx) * kColWords + pt,
+                                    -(long long)ntx * kColWords, ty);
+            Chain colQ = make_chain(ws.col + (long long)((int)tile - ntx) * kColWords + kTileW + pt,
+                                    -(long long)ntx * kColWords, ty);
+            Backoff bo;
+            bool ok = true;
             {
-                uint32_t eI = sumI, eQ = sumQ;  // inclusive lane scan, then exclusive
+                uint64_t wr[kRowWindow], w0[kColWindowEarly], w1[kColWindowEarly];
+                chain_load(row, wr);
+                chain_load(colS, w0);
+                chain_load(colQ, w1);
+                // Column sums over the warp's 32 rows of the row prefixes
+                // within the warp's part of the tile: the prefix at (row k,
+                // lane L, column c) is (sum of row k's lanes < L) + (lane L's
+                // pixels up to c), so its sum over the rows is one exclusive
+                // lane scan of the lanes' 32-row totals plus the prefix sums
+                // of the lane's per-column totals.  Per-column totals of two
+                // byte lanes share a 32-bit word (at most 32 * 255 each).
+                uint32_t b02 = 0, b13 = 0, q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+#pragma unroll 8
+                for (int k = 0; k < kRowsPerWarp; ++k) {
+                    const uint32_t v =
+                        *reinterpret_cast<const uint32_t *>(&s_pix[ps][warp * kRowsPerWarp + k][4 * lane]);
+                    b02 += __byte_perm(v, 0u, 0x4240);
+                    b13 += __byte_perm(v, 0u, 0x4341);
+                    const uint32_t x0 = v & 255u, x1 = (v >> 8) & 255u, x2 = (v >> 16) & 255u, x3 = v >> 24;
+                    q0 += x0 * x0; q1 += x1 * x1; q2 += x2 * x2; q3 += x3 * x3;
+                }
+                uint32_t cI[4], cQ[4];
+                cI[0] = b02 & 0xffffu;
+                cI[1] = cI[0] + (b13 & 0xffffu);
+                cI[2] = cI[1] + (b02 >> 16);
+                cI[3] = cI[2] + (b13 >> 16);
+                cQ[0] = q0; cQ[1] = q0 + q1; cQ[2] = cQ[1] + q2; cQ[3] = cQ[2] + q3;
+                uint32_t eI = cI[3], eQ = cQ[3];  // inclusive lane scan, then exclusive
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const uint32_t tI = __shfl_up_sync(0xffffffffu, eI, o);
                     const uint32_t tQ = __shfl_up_sync(0xffffffffu, eQ, o);
                     if (lane >= o) { eI += tI; eQ += tQ; }
                 }
-                eI -= sumI;
-                eQ -= sumQ;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) { cI[c] += eI; cQ[c] += eQ; }
-            }
-            {
+                eI -= cI[3];
+                eQ -= cQ[3];
+                // the lane-local prefix is summed over 32 rows; the lanes to
+                // the left contribute their 32-row totals to every column
                 uint4 *dst = reinterpret_cast<uint4 *>(&s_colPart[warp][4 * lane]);
-                dst[0] = make_uint4(cI[0], cQ[0], cI[1], cQ[1]);
-                dst[1] = make_uint4(cI[2], cQ[2], cI[3], cQ[3]);
+                dst[0] = make_uint4(cI[0] + eI, cQ[0] + eQ, cI[1] + eI, cQ[1] + eQ);
+                dst[1] = make_uint4(cI[2] + eI, cQ[2] + eQ, cI[3] + eI, cQ[3] + eQ);
+                const bool moved = chain_take(row, wr, epoch);
+                chain_take(colS, w0, epoch);
+                chain_take(colQ, w1, epoch);
+                if (!row.done && !moved) ok = bo.wait(cx);
             }
-            named_bar_sync(kBarProd, kProducers);
-
-            // 3. row carries (one row per producer thread): publish this tile's
-            //    row sums, look back to the left
+            while (ok && !row.done) {
+                uint64_t wr[kRowWindow], w0[kColWindowEarly], w1[kColWindowEarly];
+                chain_load(row, wr);
+                chain_load(colS, w0);
+                chain_load(colQ, w1);
+                const bool moved = chain_take(row, wr, epoch);
+                chain_take(colS, w0, epoch);
+                chain_take(colQ, w1, epoch);
+                if (!row.done && !moved) ok = bo.wait(cx);
+            }
+            if (!ok) s_fail = 1;
+            else if (tx > 0 && publish) st_relaxed_u64(rowMine, make_word(epoch, FLAG_PREFIX, row.acc + rowV));
             {
-                const uint2 tot = s_rowTot[pt];
-                const uint64_t v = (uint64_t)tot.x | ((uint64_t)tot.y << kRowQShift);
-                uint64_t *mine = ws.row + (size_t)tile * kTileH + pt;
-                if (publish)
-                    st_relaxed_u64(mine, make_word(epoch, tx == 0 ? FLAG_PREFIX : FLAG_AGGREGATE, v));
-                uint64_t carry = 0;
-                if (tx > 0) {
-                    if (look_back(ws.row + pt, kTileH, (int)tile - 1, 1, tx, carry, cx)) {
-                        if (publish) st_relaxed_u64(mine, make_word(epoch, FLAG_PREFIX, carry + v));
-                    } else {
-                        s_fail = 1;
-                    }
-                }
-                const uint2 rc = make_uint2((uint32_t)(carry & ((1u << kRowQShift) - 1u)),
-                                            (uint32_t)(carry >> kRowQShift));
-                s_rowCarry[pt] = rc;
-                S_.rowCarry[pt] = rc;
-            }
-            named_bar_sync(kBarProd, kProducers);
-            if (s_fail) {
-                if (pt == 0) {
-                    unsigned t = s_next;
-                    while (t < (unsigned)ntiles) t = grab();  // keep the ticket count exact
-                    S_.tile = kStageAbort;
-                }
-                named_bar_arrive(kBarFull0 + sb, kThreads);
-                break;
-            }
-            // 4. per-warp sums of the row carries
-            {
-                long long a = 0, b = 0;
-                if (lane < kRowsPerWarp) {
-                    const uint2 c = s_rowCarry[warp * kRowsPerWarp + lane];
-                    a = c.x;
-                    b = c.y;
-                }
+                const uint64_t carry = ok ? row.acc : 0ull;
+                const uint32_t rcI = (uint32_t)(carry & ((1u << kRowQShift) - 1u));
+                const uint32_t rcQ = (uint32_t)(carry >> kRowQShift);
+                S_.rowCarry[pt] = make_uint2(rcI, rcQ);
+                // 4. per-warp sums of the row carries
+                long long a = rcI, b = rcQ;
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) {
                     a += __shfl_xor_sync(0xffffffffu, a, o);
@@ -459,53 +523,59 @@ sat_build_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__rest
                 if (lane == 0) { s_warpCarry[warp][0] = a; s_warpCarry[warp][1] = b; }
             }
             named_bar_sync(kBarProd, kProducers);
-            // 5. column carries: thread = column, both tables together
+            if (s_fail) {
+                if (pt == 0) S_.tile = kStageAbort;
+                named_bar_arrive(kBarFull0 + sb, kThreads);
+                break;
+            }
+            // 5. column carries: thread = column, both tables together.  The
+            //    column sums include the row carries, so they are published
+            //    only now: as an inclusive prefix when the look-back above
+            //    already ended, else as an aggregate until it does.
             {
                 const int c = pt;
-                long long part[kGroups][2];
                 long long agg[2] = {0, 0};
 #pragma unroll
                 for (int w = 0; w < kGroups; ++w) {
                     const uint2 cp = s_colPart[w][c];
-                    part[w][0] = (long long)cp.x + s_warpCarry[w][0];
-                    part[w][1] = (long long)cp.y + s_warpCarry[w][1];
-                    agg[0] += part[w][0];
-                    agg[1] += part[w][1];
+                    agg[0] += (long long)cp.x + s_warpCarry[w][0];
+                    agg[1] += (long long)cp.y + s_warpCarry[w][1];
                 }
                 uint64_t *mine = ws.col + (size_t)tile * kColWords + c;
+                const bool early = colS.done && colQ.done;  // ty == 0 included
                 if (publish) {
-                    const uint32_t state = ty == 0 ? FLAG_PREFIX : FLAG_AGGREGATE;
-                    st_relaxed_u64(mine, make_word(epoch, state, (uint64_t)agg[0]));
-                    st_relaxed_u64(mine + kTileW, make_word(epoch, state, (uint64_t)agg[1]));
+                    const uint32_t state = early ? FLAG_PREFIX : FLAG_AGGREGATE;
+                    const uint64_t b0 = early ? colS.acc : 0ull, b1 = early ? colQ.acc : 0ull;
+                    st_relaxed_u64(mine, make_word(epoch, state, b0 + (uint64_t)agg[0]));
+                    st_relaxed_u64(mine + kTileW, make_word(epoch, state, b1 + (uint64_t)agg[1]));
                 }
-                uint64_t carry0 = 0, carry1 = 0;
-                if (ty > 0) {
-                    if (look_back2(ws.col + c, ws.col + kTileW + c, kColWords, (int)tile - ntx, ntx,
-                                   ty, carry0, carry1, cx)) {
-                        if (publish) {
-                            st_relaxed_u64(mine, make_word(epoch, FLAG_PREFIX, carry0 + (uint64_t)agg[0]));
-                            st_relaxed_u64(mine + kTileW, make_word(epoch, FLAG_PREFIX, carry1 + (uint64_t)agg[1]));
-                        }
-                    } else {
-                        s_fail = 1;
-                    }
+                bool ok = true;
+                while (!colS.done || !colQ.done) {
+                    uint64_t w0[kColWindow], w1[kColWindow];
+                    chain_load(colS, w0);
+                    chain_load(colQ, w1);
+                    const bool moved = chain_take(colS, w0, epoch) | chain_take(colQ, w1, epoch);
+                    if ((!colS.done || !colQ.done) && !moved && !bo.wait(cx)) { ok = false; break; }
                 }
-                long long run0 = (long long)carry0, run1 = (long long)carry1;
+                if (!ok) {
+                    s_fail = 1;
+                } else if (!early && publish) {
+                    st_relaxed_u64(mine, make_word(epoch, FLAG_PREFIX, colS.acc + (uint64_t)agg[0]));
+                    st_relaxed_u64(mine + kTileW, make_word(epoch, FLAG_PREFIX, colQ.acc + (uint64_t)agg[1]));
+                }
+                long long run0 = (long long)colS.acc, run1 = (long long)colQ.acc;
 #pragma unroll
                 for (int g = 0; g < kGroups; ++g) {
                     S_.colStart[g][0][c] = run0;
                     S_.colStart[g][1][c] = run1;
-                    run0 += part[g][0];
-                    run1 += part[g][1];
+                    const uint2 cp = s_colPart[g][c];
+                    run0 += (long long)cp.x + s_warpCarry[g][0];
+                    run1 += (long long)cp.y + s_warpCarry[g][1];
                 }
             }
             named_bar_sync(kBarProd, kProducers);
             const bool failed = s_fail != 0;
             if (pt == 0) {
-                if (failed) {
-                    unsigned t = s_next;
-                    while (t < (unsigned)ntiles) t = grab();
-                }
                 S_.tile = failed ? kStageAbort : (int)tile;
                 S_.pix = ps;
             }
@@ -546,33 +616,46 @@ sat_build_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__rest
                 runI[c] = S_.colStart[g][0][4 * lane + c];
                 runQ[c] = S_.colStart[g][1][4 * lane + c];
             }
-#pragma unroll 4
-            for (int k = 0; k < kRowsPerWarp; ++k) {
-                const int r = g * kRowsPerWarp + k, y = ty * kTileH + r;
-                if (y >= H) break;
-                const uint2 rc = S_.rowCarry[r];
-                uint32_t pI[4], pQ[4];
-                row_scan(*reinterpret_cast<const uint32_t *>(&s_pix[ps][r][4 * lane]), lane, pI, pQ);
+            // four rows at a time: their lane scans are independent, so
+            // their shuffle chains overlap.  Rows past the image bottom are
+            // zeros in the stage and only their stores are skipped.
+#pragma unroll 1
+            for (int k0 = 0; k0 < kRowsPerWarp; k0 += kScanRows) {
+                const int r0 = g * kRowsPerWarp + k0, y0 = ty * kTileH + r0;
+                uint32_t px[kScanRows];
+                uint2 rc[kScanRows];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    runI[c] += (uint32_t)(rc.x + pI[c]);
-                    runQ[c] += (uint32_t)(rc.y + pQ[c]);
+                for (int j = 0; j < kScanRows; ++j) {
+                    px[j] = *reinterpret_cast<const uint32_t *>(&s_pix[ps][r0 + j][4 * lane]);
+                    rc[j] = S_.rowCarry[r0 + j];
                 }
-                const size_t o = (size_t)y * W + xl;
-                if (kStore == 2 && xl + 3 < W) {
-                    st_v4_b64(S + o, runI[0], runI[1], runI[2], runI[3]);
-                    st_v4_b64(Q + o, runQ[0], runQ[1], runQ[2], runQ[3]);
-                } else if (kStore == 1 && xl + 3 < W) {
-                    __stcs(reinterpret_cast<longlong2 *>(S + o), make_longlong2(runI[0], runI[1]));
-                    __stcs(reinterpret_cast<longlong2 *>(S + o + 2), make_longlong2(runI[2], runI[3]));
-                    __stcs(reinterpret_cast<longlong2 *>(Q + o), make_longlong2(runQ[0], runQ[1]));
-                    __stcs(reinterpret_cast<longlong2 *>(Q + o + 2), make_longlong2(runQ[2], runQ[3]));
-                } else {
+                uint32_t pI[kScanRows][4], pQ[kScanRows][4];
+                row_scan_rows(px, lane, pI, pQ);
+#pragma unroll
+                for (int j = 0; j < kScanRows; ++j) {
+                    const int y = y0 + j;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        if (xl + c < W) {
-                            S[o + c] = runI[c];
-                            Q[o + c] = runQ[c];
+                        runI[c] += (uint32_t)(rc[j].x + pI[j][c]);
+                        runQ[c] += (uint32_t)(rc[j].y + pQ[j][c]);
+                    }
+                    if (y >= H) continue;
+                    const size_t o = (size_t)y * W + xl;
+                    if (kStore == 2 && xl + 3 < W) {
+                        st_v4_b64(S + o, runI[0], runI[1], runI[2], runI[3]);
+                        st_v4_b64(Q + o, runQ[0], runQ[1], runQ[2], runQ[3]);
+                    } else if (kStore == 1 && xl + 3 < W) {
+                        __stcs(reinterpret_cast<longlong2 *>(S + o), make_longlong2(runI[0], runI[1]));
+                        __stcs(reinterpret_cast<longlong2 *>(S + o + 2), make_longlong2(runI[2], runI[3]));
+                        __stcs(reinterpret_cast<longlong2 *>(Q + o), make_longlong2(runQ[0], runQ[1]));
+                        __stcs(reinterpret_cast<longlong2 *>(Q + o + 2), make_longlong2(runQ[2], runQ[3]));
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            if (xl + c < W) {
+                                S[o + c] = runI[c];
+                                Q[o + c] = runQ[c];
+                            }
                         }
                     }
                 }
@@ -580,9 +663,31 @@ sat_build_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__rest
             named_bar_arrive(kBarEmpty0 + sb, kThreads);  // the stage may be refilled
         }
     }
+    // The last CTA out returns the dispenser and the SM counters to zero for
+    // the next launch on this workspace (every CTA has drawn its last ticket
+    // before it counts itself done).
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        s_last = atomicAdd(ws.done, 1u) == gridDim.x - 1 ? 1 : 0;
+    }
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        for (int k = tid; k < kMaxSmIds; k += kThreads) ws.smTiles[k] = 0u;
+        if (tid == 0) {
+            *ws.ticket = 0ull;
+            *ws.done = 0u;
+        }
+    }
 }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Workspace: ticket (8 bytes), abort word, done count; the SM counters from
+// byte 256; the row words, then the column words.
+constexpr size_t kHeaderBytes = 256 + kMaxSmIds * sizeof(unsigned);
+static_assert(kHeaderBytes % 256 == 0, "row words stay 256-byte aligned");
 
 // Library-owned look-back workspace, one per device.  Calls on different
 // streams are ordered through `last` so they never use it concurrently.
@@ -590,7 +695,6 @@ struct DeviceWs {
     void *ptr = nullptr;
     size_t bytes = 0;
     uint32_t epoch = 0;
-    unsigned long long ticket_base = 0;
     bool dirty = false;
     bool used = false;
     cudaEvent_t last = nullptr;
@@ -609,35 +713,40 @@ SatPlan sat_plan(int W, int H) {
     p.ntx = (W + kTileW - 1) / kTileW;
     p.nty = (H + kTileH - 1) / kTileH;
     const size_t nt = (size_t)p.ntx * p.nty;
-    p.zero_bytes = 256;                                       // ticket and abort word
-    p.total_bytes = 256 + align_up(nt * kTileH * 8, 256) + align_up(nt * kColWords * 8, 256);
+    p.zero_bytes = kHeaderBytes;  // dispenser, abort word, done count, SM counters
+    p.total_bytes = kHeaderBytes + align_up(nt * kTileH * 8, 256) + align_up(nt * kColWords * 8, 256);
     return p;
 }
 
-// Persistent grid: as many rounds as the resident CTAs need, and the tiles
-// spread evenly over them, so no CTA runs a last round alone.
-int persistent_grid(int ntiles) {
+int sm_count() {
     static int sms[kMaxDevices] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 1;
     if (!sms[dev] && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return 1;
-    const int resident = sms[dev] * kCtasPerSm;
-    const int rounds = (ntiles + resident - 1) / resident;
-    return (ntiles + rounds - 1) / rounds;
+    return sms[dev] > 0 ? sms[dev] : 1;
+}
+
+// Persistent grid: the same number of CTAs on every SM (kCtasPerSm, or one
+// CTA per tile for small images); the kernel's share rule then spreads the
+// tiles evenly over the SMs.
+int persistent_grid(int ntiles, int nsm) {
+    const int resident = nsm * kCtasPerSm;
+    return ntiles < resident ? ntiles : resident;
 }
 
 cudaError_t sat_launch(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
-                       void *workspace, const SatPlan &plan, uint32_t epoch,
-                       unsigned long long ticket_base, int *status, uint64_t timeout_ns,
-                       int fault_tile, cudaStream_t stream, unsigned long long *tickets_used) {
+                       void *workspace, const SatPlan &plan, uint32_t epoch, int *status,
+                       uint64_t timeout_ns, int fault_tile, cudaStream_t stream) {
     const size_t nt = (size_t)plan.ntx * plan.nty;
     char *base = static_cast<char *>(workspace);
     SatWs ws;
     ws.ticket = reinterpret_cast<unsigned long long *>(base);
     ws.abort = reinterpret_cast<unsigned *>(base + 8);
-    ws.row = reinterpret_cast<uint64_t *>(base + 256);
-    ws.col = reinterpret_cast<uint64_t *>(base + 256 + align_up(nt * kTileH * 8, 256));
+    ws.done = reinterpret_cast<unsigned *>(base + 12);
+    ws.smTiles = reinterpret_cast<unsigned *>(base + 256);
+    ws.row = reinterpret_cast<uint64_t *>(base + kHeaderBytes);
+    ws.col = reinterpret_cast<uint64_t *>(base + kHeaderBytes + align_up(nt * kTileH * 8, 256));
 
     const bool aligned4 = (W % 4 == 0) && ((uintptr_t)img % 4 == 0);
     const int store = ((W % 4 == 0) && ((uintptr_t)S % 32 == 0) && ((uintptr_t)Q % 32 == 0)) ? 2
@@ -658,7 +767,9 @@ cudaError_t sat_launch(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
     } else {
         tma = false;
     }
-    const int grid = persistent_grid((int)nt);
+    const int nsm = sm_count();
+    const int grid = persistent_grid((int)nt, nsm);
+    const int smCap = (int)((nt + nsm - 1) / nsm);  // tiles per SM, rounded up
     long long *s = reinterpret_cast<long long *>(S), *q = reinterpret_cast<long long *>(Q);
     const int dyn = kPixSlots * kTileH * kTileW + 128;
 #define NCC_SAT(T, A, V)                                                                        \
@@ -668,7 +779,7 @@ cudaError_t sat_launch(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
         if (ea != cudaSuccess) return ea;                                                       \
         sat_build_kernel<T, A, V><<<grid, kThreads, dyn, stream>>>(tmap, img, W, H, s, q, ws,   \
                                                                    plan.ntx, (int)nt, epoch,    \
-                                                                   ticket_base, status,         \
+                                                                   nsm, smCap, kShareQ, status, \
                                                                    timeout_ns, fault_tile);     \
     } while (0)
     if (tma && store == 2) NCC_SAT(true, true, 2);
@@ -679,8 +790,6 @@ cudaError_t sat_launch(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
     else if (store == 1) NCC_SAT(false, false, 1);
     else NCC_SAT(false, false, 0);
 #undef NCC_SAT
-    // every CTA takes tickets until it draws one past the last tile
-    if (tickets_used) *tickets_used = (unsigned long long)nt + (unsigned long long)grid;
     return cudaGetLastError();
 }
 
@@ -712,7 +821,6 @@ cudaError_t sat_build_run(const uint8_t *img, int W, int H, int64_t *S, int64_t 
         if (e != cudaSuccess) return e;
         d.bytes = bytes;
         d.epoch = 0;
-        d.ticket_base = 0;
         d.dirty = false;
     }
     if (d.used && d.last_stream != stream) {
@@ -724,18 +832,14 @@ cudaError_t sat_build_run(const uint8_t *img, int W, int H, int64_t *S, int64_t 
         e = cudaMemsetAsync(d.ptr, 0, d.bytes, stream);
         if (e != cudaSuccess) return e;
         d.epoch = 0;
-        d.ticket_base = 0;
         d.dirty = false;
     }
     d.epoch += 1;
-    unsigned long long used = 0;
-    e = sat_launch(img, W, H, S, Q, d.ptr, plan, d.epoch, d.ticket_base, status, timeout_ns,
-                   fault_tile, stream, &used);
+    e = sat_launch(img, W, H, S, Q, d.ptr, plan, d.epoch, status, timeout_ns, fault_tile, stream);
     if (e != cudaSuccess) {
-        d.dirty = true;  // the ticket count is unknown: clear before the next use
+        d.dirty = true;  // whether the kernel ran is unknown: clear before the next use
         return e;
     }
-    d.ticket_base += used;
     e = cudaEventRecord(d.last, stream);
     d.last_stream = stream;
     d.used = true;

@@ -85,8 +85,7 @@ extern "C" int ncc_sat_build_noalloc(const uint8_t *img, int W, int H, int64_t *
     // The previous call's look-back words are still in the array: clear the
     // whole region this image uses so every word reads as not yet published.
     if (cudaMemsetAsync(scratch, 0, plan.total_bytes, st) != cudaSuccess) return NCC_ERR_CUDA;
-    const cudaError_t e = ncc::sat_launch(img, W, H, S, Q, scratch, plan, /*epoch=*/1u,
-                                          /*ticket_base=*/0ull, status, kTimeoutNs,
-                                          /*fault_tile=*/-1, st);
+    const cudaError_t e = ncc::sat_launch(img, W, H, S, Q, scratch, plan, /*epoch=*/1u, status,
+                                          kTimeoutNs, /*fault_tile=*/-1, st);
     return e == cudaSuccess ? NCC_OK : NCC_ERR_CUDA;
 }
