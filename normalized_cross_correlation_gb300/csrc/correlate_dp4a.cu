@@ -39,8 +39,10 @@
 //     / column -1 = 0.  (Tables whose rows are not a multiple of 16 bytes, or
 //     templates wider than 127, read the corners with global loads.)  The
 //     four-corner sums use the low 32 bits of the table entries (exact: the
-//     sums are below 2^32); templates of at most 258 pixels compute the
-//     coefficient in fp32 with exact products, larger ones in exact int64.
+//     sums are below 2^32); templates of at most 363 pixels form the
+//     coefficient's numerator and variance terms exactly in 32-bit integers
+//     (their magnitude is at most N^2 * 127.5^2 < 2^31), larger ones in
+//     exact int64; each term is rounded to fp32 once.
 #include "ncc_common.cuh"
 
 #include <cuda.h>
@@ -60,6 +62,11 @@ constexpr int kMaxSmem = 227 * 1024;   // opt-in shared memory per CTA
 constexpr int kEpiStages = 2;          // table-row staging ring depth
 constexpr int kEpiRowsPerStep = 4;     // output rows per epilogue step (rows per TMA box)
 constexpr int kEpiBufs = 4;            // boxes per stage: S top, S bottom, Q top, Q bottom
+// Templates of at most this many pixels form the coefficient's numerator
+// N*SumIT - SumI*SumT and variance term N*SumI2 - SumI^2 in 32-bit integers:
+// both are N^2 times a covariance or variance of values in 0..255, so at
+// most N^2 * 127.5^2 < 2^31 in magnitude.
+constexpr long long kMaxInt32N = 363;
 
 struct Geom {
     int nch;         // 16-pixel template chunks
@@ -98,6 +105,11 @@ struct KParams {
     int *status;
     int Ox, Oy;
     Geom g;
+};
+
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -228,6 +240,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     unsigned sa = 0, sb = 0;    // SumT < 2^25 and SumT2 < 2^32 (wT*hT <= 66051)
     for (int wi = tid; wi < nWords; wi += kThreads) {
         const int j = wi / (g.nch * 4), cw = wi - j * g.nch * 4;
+        const int slot = ((cw >> 2) * p.hT + j) * 4 + (cw & 3);  // chunk-major
         uint32_t v = 0;
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
@@ -239,7 +252,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                 sb += t * t;
             }
         }
-        tw[wi] = v;
+        tw[slot] = v;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -275,7 +288,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
 
     for (int c = 0; c < g.nch; ++c) {
         const uint8_t *cc = cp + 16 * c + warp * kRowsPerThread * g.boxW;
-        const uint4 *tc = reinterpret_cast<const uint4 *>(tw) + c;  // chunk c of row j at tc[j*nch]
+        const uint4 *tc = reinterpret_cast<const uint4 *>(tw) + c * p.hT;  // chunk c of row j at tc[j]
         // the d-shifted words of tile row r of this warp
         auto row_words = [&](int r, uint32_t (&v)[7]) {
             const uint8_t *rp = cc + r * g.boxW;
@@ -306,13 +319,13 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                 uint32_t v[7];
                 row_words(r, v);
 #pragma unroll
-                for (int i = 0; i <= r; ++i) mac(acc[i], v, tc[(r - i) * g.nch]);
+                for (int i = 0; i <= r; ++i) mac(acc[i], v, tc[r - i]);
             }
             for (int r = kRowsPerThread - 1; r < p.hT; ++r) {
                 uint32_t v[7];
                 row_words(r, v);
 #pragma unroll
-                for (int i = 0; i < kRowsPerThread; ++i) mac(acc[i], v, tc[(r - i) * g.nch]);
+                for (int i = 0; i < kRowsPerThread; ++i) mac(acc[i], v, tc[r - i]);
             }
 #pragma unroll
             for (int m = 0; m < kRowsPerThread - 1; ++m) {
@@ -320,7 +333,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                 uint32_t v[7];
                 row_words(r, v);
 #pragma unroll
-                for (int i = m + 1; i < kRowsPerThread; ++i) mac(acc[i], v, tc[(r - i) * g.nch]);
+                for (int i = m + 1; i < kRowsPerThread; ++i) mac(acc[i], v, tc[r - i]);
             }
         } else {
             const int rows = kRowsPerThread + p.hT - 1;
@@ -330,7 +343,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
 #pragma unroll
                 for (int i = 0; i < kRowsPerThread; ++i) {
                     const int j = r - i;
-                    if (j >= 0 && j < p.hT) mac(acc[i], v, tc[j * g.nch]);
+                    if (j >= 0 && j < p.hT) mac(acc[i], v, tc[j]);
                 }
             }
         }
@@ -349,17 +362,21 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     // --- epilogue: moments from S and Q, coefficient -----------------------
     // The four-corner sums are below 2^32, so they are formed from the low
     // 32 bits of the table entries with wrapping arithmetic, exactly.  For
-    // templates of at most 258 pixels every integer involved is below 2^24
-    // and the coefficient is computed in fp32 with exact products (fma
-    // splits); larger templates take exact 64-bit integers.
+    // templates of at most kMaxInt32N pixels the numerator and variance
+    // terms are exact 32-bit integers; larger templates take exact 64-bit
+    // integers.
     const long long N = (long long)p.wT * p.hT;
     const long long sT = s_sumT, vT = s_vT;
     const float invSqrtVT = s_invSqrtVT;
-    const bool smallN = N <= 258;
-    const float Nf = (float)N, sTf = (float)sT;  // exact when smallN
+    const bool smallN = N <= kMaxInt32N;
+    const uint32_t Nu = (uint32_t)N, sTu = (uint32_t)sT;
     const int h = warp >> 2, xo = (warp & 3) * 32 + lane, x = x0 + xo;
     const int segWords = g.epiBW * 2;                          // u32 words per table-row segment
     const int cl = 2 * (xo + 1), cr = 2 * (xo + p.wT + 1);      // low words of x-1, x+wT-1
+    // the loop is instantiated once per coefficient path, so neither body
+    // carries the other's code
+    auto epilogue = [&](auto smallTag) {
+    constexpr bool kSmall = decltype(smallTag)::value;
     for (int t = 0; t < epiSteps; ++t) {
         const int st = t % kEpiStages;
         const uint32_t par = (uint32_t)((t / kEpiStages) & 1);
@@ -407,18 +424,13 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
             } else {
                 float num, vIf;
                 bool vIpos;
-                if (smallN) {
-                    // exact N*SumIT - SumI*SumT and N*SumI2 - SumI^2 up to their
-                    // final roundings: both products split exactly by fma, the
-                    // high parts cancel exactly when they are close
-                    const float sit = (float)sumIT, sIf = (float)sI, sI2f = (float)sI2;
-                    const float p1 = Nf * sit, e1 = fmaf(Nf, sit, -p1);
-                    const float p2 = sIf * sTf, e2 = fmaf(sIf, sTf, -p2);
-                    num = (p1 - p2) + (e1 - e2);
-                    const float q1 = Nf * sI2f, f1 = fmaf(Nf, sI2f, -q1);
-                    const float q2 = sIf * sIf, f2 = fmaf(sIf, sIf, -q2);
-                    vIf = (q1 - q2) + (f1 - f2);
-                    vIpos = vIf > 0.f;
+                if (kSmall) {
+                    // both terms exactly by wrapping 32-bit products, then
+                    // one rounding each
+                    num = (float)(int)(Nu * sumIT - sI * sTu);
+                    const uint32_t vIu = Nu * sI2 - sI * sI;
+                    vIpos = vIu != 0u;
+                    vIf = (float)vIu;
                 } else {
                     // SumI < 2^25 and SumT < 2^25; SumI2 < 2^32
                     const long long numi = (long long)((unsigned long long)N * sumIT) -
@@ -443,6 +455,9 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
             issue_epi(t + kEpiStages);
         }
     }
+    };
+    if (smallN) epilogue(BoolTag<true>{});
+    else epilogue(BoolTag<false>{});
 }
 
 }  // namespace

@@ -42,6 +42,8 @@ CASES = [  # (W, H, wT, hT)
     (40, 30, 1, 1), (50, 41, 3, 5), (300, 200, 16, 16), (257, 190, 17, 9),
     (400, 333, 32, 32), (600, 300, 64, 64), (129, 77, 129, 1), (93, 150, 1, 150),
     (64, 64, 64, 64), (1000, 260, 13, 31), (272, 96, 100, 40), (513, 70, 128, 20),
+    # grouped table-row loads: partial last block of 4*hT rows, views shifted by H mod hT
+    (512, 300, 12, 7), (256, 157, 8, 15), (320, 133, 20, 2),
 ]
 
 
