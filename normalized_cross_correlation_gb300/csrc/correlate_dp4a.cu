@@ -124,6 +124,14 @@ __device__ __forceinline__ float u64_to_f32(unsigned long long a) {
                 __uint2float_rn((unsigned)a));
 }
 
+// 1/sqrt(v) from the hardware approximation (relative error about 2^-22.9),
+// flushing subnormals: v is an integer >= 1 here.
+__device__ __forceinline__ float rsqrt_approx(float v) {
+    float r;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 __device__ __forceinline__ float i64_to_f32(long long v) {
     const float f = u64_to_f32(v < 0 ? (unsigned long long)(-v) : (unsigned long long)v);
     return v < 0 ? -f : f;
@@ -373,10 +381,10 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     const int h = warp >> 2, xo = (warp & 3) * 32 + lane, x = x0 + xo;
     const int segWords = g.epiBW * 2;                          // u32 words per table-row segment
     const int cl = 2 * (xo + 1), cr = 2 * (xo + p.wT + 1);      // low words of x-1, x+wT-1
-    // the loop is instantiated once per coefficient path, so neither body
-    // carries the other's code
-    auto epilogue = [&](auto smallTag) {
-    constexpr bool kSmall = decltype(smallTag)::value;
+    // the loop is instantiated per coefficient path and for full tiles
+    // (every output row and column valid: no per-output bounds checks)
+    auto epilogue = [&](auto smallTag, auto fullTag) {
+    constexpr bool kSmall = decltype(smallTag)::value, kFull = decltype(fullTag)::value;
     for (int t = 0; t < epiSteps; ++t) {
         const int st = t % kEpiStages;
         const uint32_t par = (uint32_t)((t / kEpiStages) & 1);
@@ -414,7 +422,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
             if (x > 0) { sI -= (uint32_t)__ldg(Sb + xl); sI2 -= (uint32_t)__ldg(Qb + xl); }
             if (x > 0 && y > 0) { sI += (uint32_t)__ldg(St + xl); sI2 += (uint32_t)__ldg(Qt + xl); }
         }
-        if (y < p.Oy && x < p.Ox) {
+        if (kFull || (y < p.Oy && x < p.Ox)) {
             const unsigned sumIT = sIT[row * kOutW + xo];
             const size_t o = (size_t)y * p.Ox + x;
             if (kMoments) {
@@ -443,7 +451,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                 }
                 float r = 0.0f;
                 if (vIpos && vT > 0) {
-                    r = num * rsqrtf(vIf) * invSqrtVT;
+                    r = num * rsqrt_approx(vIf) * invSqrtVT;
                     r = fminf(1.0f, fmaxf(-1.0f, r));
                 }
                 __stcs(p.out + o, r);
@@ -456,8 +464,10 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         }
     }
     };
-    if (smallN) epilogue(BoolTag<true>{});
-    else epilogue(BoolTag<false>{});
+    const bool full = y0 + kOutH <= p.Oy && x0 + kOutW <= p.Ox;
+    if (smallN && full) epilogue(BoolTag<true>{}, BoolTag<true>{});
+    else if (smallN) epilogue(BoolTag<true>{}, BoolTag<false>{});
+    else epilogue(BoolTag<false>{}, BoolTag<false>{});
 }
 
 }  // namespace
