@@ -45,6 +45,11 @@
 namespace ncc {
 namespace {
 
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
+
 constexpr int kThreads = 384;
 constexpr int kM = 128;               // shifts per tile (MMA M)
 constexpr int kTY = 32;               // output rows per tile
@@ -56,6 +61,7 @@ constexpr int kMaxSmem = 110 * 1024;  // two CTAs per SM
 constexpr int kMaxTmemCols = 256;     // per CTA (two CTAs share 512 columns)
 
 struct BankGeom {
+    bool pair;      // two output rows per accumulator (see the pair mode below)
     int nTpad;      // templates padded to a multiple of 32 (MMA N; 32-column TMEM loads)
     int nK16;       // 16-column template chunks (MMA K steps per template row)
     int G;          // template rows per exact accumulator group
@@ -76,15 +82,25 @@ int pow2_at_least(int v) {
     return p;
 }
 
-bool make_geom(int wT, int hT, int nT, BankGeom &g) {
+// Pair mode (one exact group, nTpad <= 64): one accumulator holds output rows
+// y and y+1 of every template (N = 2*nTpad).  Image row y+d meets template
+// row d for output row y and template row d-1 for output row y+1, so one MMA
+// per image row d = 0..hT serves both rows: hT+1 MMAs per two output rows
+// instead of 2*hT.  B is stored with the template rows upside down between
+// two zero blocks -- block b holds template row hT-b, blocks 0 and hT+1 are
+// zero -- in the layout [K chunk][K half][block][template][8 k], so the
+// operand of image row d is the two consecutive blocks hT-d, hT-d+1.
+bool make_geom(int wT, int hT, int nT, bool pair, BankGeom &g) {
     if (wT > kMaxExactPixels) return false;
+    g.pair = pair;
     g.nTpad = (nT + 31) / 32 * 32;
     if (g.nTpad > 256) return false;
     g.nK16 = (wT + 15) / 16;
     g.G = kMaxExactPixels / wT;
     if (g.G > hT) g.G = hT;
     g.nG = (hT + g.G - 1) / g.G;
-    g.accCols = g.nTpad * g.nG;
+    if (pair && (g.nG != 1 || g.nTpad > 64)) return false;
+    g.accCols = g.nTpad * g.nG * (pair ? 2 : 1);
     if (g.accCols > kMaxTmemCols) return false;
     g.na = kMaxTmemCols / g.accCols;
     if (g.na > 4) g.na = 4;
@@ -93,7 +109,7 @@ bool make_geom(int wT, int hT, int nT, BankGeom &g) {
     g.xBlocks = 15 + 2 * g.nK16;
     g.xBytes = g.xBlocks * 128;
     g.nx = hT + 4;
-    g.bBytes = hT * g.nK16 * g.nTpad * 32;
+    g.bBytes = pair ? g.nK16 * 2 * (hT + 2) * g.nTpad * 16 : hT * g.nK16 * g.nTpad * 32;
     g.offB = 0;
     g.offX = (g.bBytes + 1023) / 1024 * 1024;
     g.offSt = g.offX + g.nx * g.xBytes;
@@ -123,6 +139,14 @@ __device__ __forceinline__ uint32_t saddr(const void *p) {
 
 __device__ __forceinline__ float u64_to_f32(unsigned long long a) {
     return fmaf(__uint2float_rn((unsigned)(a >> 32)), 4294967296.0f, __uint2float_rn((unsigned)a));
+}
+
+// 1/sqrt(v) from the hardware approximation (relative error about 2^-22.9),
+// flushing subnormals: v is an integer >= 1 here.
+__device__ __forceinline__ float rsqrt_approx(float v) {
+    float r;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
 }
 
 __device__ __forceinline__ float i64_to_f32(long long v) {
@@ -220,7 +244,7 @@ __device__ __forceinline__ uint32_t bytes_to_h2(uint32_t w, uint32_t sel) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <bool kMoments, bool kOneGroup>
+template <bool kMoments, bool kOneGroup, bool kPair>
 __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -238,17 +262,21 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
     // --- prologue: B operand, template statistics, barriers, tensor memory ---
     {
         const int perRow = g.nK16 * g.nTpad * 16;  // f16 elements per template row
-        const int total = p.hT * perRow;
+        const int total = (kPair ? p.hT + 2 : p.hT) * perRow;
         for (int e = tid; e < total; e += kThreads) {
-            const int j = e / perRow, rem = e - j * perRow;
+            const int jb = e / perRow, rem = e - jb * perRow;
             const int c = rem / (g.nTpad * 16), r2 = rem - c * g.nTpad * 16;
             const int n = r2 >> 4, k = r2 & 15;
             const int col = 16 * c + k;
-            const float v = (n < p.nT && col < p.wT)
+            // pair mode: block jb holds template row hT - jb (blocks 0, hT+1 zero)
+            const int j = kPair ? p.hT - jb : jb;
+            const float v = (j >= 0 && j < p.hT && n < p.nT && col < p.wT)
                                 ? (float)__ldg(p.tmpl + ((size_t)n * p.hT + j) * p.wT + col) : 0.f;
-            // K-major core matrices: (k/8) * nTpad*16 + (n/8) * 128 + (n%8) * 16 + (k%8) * 2
-            const int off = (j * g.nK16 + c) * g.nTpad * 32 + (k >> 3) * g.nTpad * 16 +
-                            (n >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2;
+            // K-major core matrices: (k/8) * (K-half stride) + (n/8) * 128 + (n%8) * 16 + (k%8) * 2
+            const int off = kPair ? ((c * 2 + (k >> 3)) * (p.hT + 2) + jb) * g.nTpad * 16 +
+                                        (n >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2
+                                  : (jb * g.nK16 + c) * g.nTpad * 32 + (k >> 3) * g.nTpad * 16 +
+                                        (n >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2;
             *reinterpret_cast<__half *>(smem + g.offB + off) = __float2half(v);
         }
         const long long N = (long long)p.wT * p.hT;
@@ -285,10 +313,11 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
     const uint32_t tmem = s_tmem;
     const long long N = (long long)p.wT * p.hT;
     // instruction descriptor: D f32, A/B f16, A MN-major, B K-major, N, M = 128
-    const uint32_t idesc = (1u << 4) | (1u << 15) | ((uint32_t)(g.nTpad >> 3) << 17) |
-                           ((uint32_t)(kM >> 4) << 24);
+    const uint32_t mmaN = kPair ? 2 * g.nTpad : g.nTpad;
+    const uint32_t idesc = (1u << 4) | (1u << 15) | ((mmaN >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
 
-    uint32_t rowSeq = 0, outSeq = 0;  // image rows / output rows handled so far (all tiles)
+    // image rows / output rows / accumulators (rows or row pairs) handled so far (all tiles)
+    uint32_t rowSeq = 0, accSeq = 0;
     for (int tile = blockIdx.x; tile < p.ntiles; tile += gridDim.x) {
         const int xt = tile % p.ntx, yb = tile / p.ntx;
         const int x0 = xt * kM, y0 = yb * kTY;
@@ -351,8 +380,41 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                 const uint32_t slot0 = rowSeq % g.nx;                           // slot of image row y0
                 uint32_t readySlot = slot0;
                 int ready = 0;  // image rows of this tile known to be converted
-                for (int yl = 0; yl < ty; ++yl) {
-                    const uint32_t o = outSeq + yl, a = o % g.na, ka = o / g.na;
+                if (kPair) {
+                    // B window of image row d: blocks hT-d and hT-d+1 (see make_geom)
+                    const uint64_t bdescP = smem_desc(saddr(smem + g.offB), (uint32_t)((p.hT + 2) * g.nTpad * 16), 128);
+                    const uint32_t bBlk = (uint32_t)(g.nTpad * 16) >> 4;
+                    const uint32_t bChunkP = (uint32_t)(2 * (p.hT + 2) * g.nTpad * 16) >> 4;
+                    for (int yl = 0; yl < ty; yl += 2) {
+                        const uint32_t o = accSeq + (uint32_t)(yl >> 1), a = o % g.na, ka = o / g.na;
+                        if (ka > 0) mbar_wait_warp(&aempty[a], (ka - 1) & 1, &s_abort, p.status);
+                        // image rows yl .. yl+hT (the last, for row yl+1 only, is skipped
+                        // when yl is the tile's last row)
+                        const int dmax = yl + 1 < ty ? p.hT : p.hT - 1;
+                        while (ready <= yl + dmax) {
+                            const uint32_t q = rowSeq + ready;
+                            mbar_wait_warp(&xfull[readySlot], (q / g.nx) & 1, &s_abort, p.status);
+                            ++ready;
+                            if (++readySlot == (uint32_t)g.nx) readySlot = 0;
+                        }
+                        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                        uint32_t s = (slot0 + yl) % g.nx;
+                        const uint32_t d = tmem + a * g.accCols;
+                        for (int dd = 0; dd <= dmax; ++dd) {
+                            const uint64_t ad = adesc0 + (uint64_t)(s * xStep);
+                            const uint64_t bd = bdescP + (uint64_t)((p.hT - dd) * bBlk);
+                            for (int c = 0; c < g.nK16; ++c)
+                                tc_mma_if(d, ad + 16u * c, bd + c * bChunkP, idesc,
+                                          (dd != 0 || c != 0) ? 1u : 0u, leader);
+                            if (++s == (uint32_t)g.nx) s = 0;
+                        }
+                        tc_commit_if(&afull[a], leader);
+                        tc_commit_if(&xempty[(slot0 + yl) % g.nx], leader);  // image rows y0+yl, y0+yl+1 done
+                        if (yl + 1 < ty) tc_commit_if(&xempty[(slot0 + yl + 1) % g.nx], leader);
+                    }
+                }
+                for (int yl = 0; yl < ty && !kPair; ++yl) {
+                    const uint32_t o = accSeq + yl, a = o % g.na, ka = o / g.na;
                     if (ka > 0) mbar_wait_warp(&aempty[a], (ka - 1) & 1, &s_abort, p.status);
                     while (ready < yl + p.hT) {
                         const uint32_t q = rowSeq + ready;
@@ -404,16 +466,24 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
             load_corners(y0);
             for (int yl = 0; yl < ty; ++yl) {
                 const int y = y0 + yl;
-                const uint32_t o = outSeq + yl, a = o % g.na, ka = o / g.na;
+                // pair mode: rows yl, yl+1 (yl even) share accumulator yl/2,
+                // row yl+1 in its second half of columns
+                const bool first = !kPair || (yl & 1) == 0;
+                const bool last = !kPair || (yl & 1) == 1 || yl + 1 == ty;
+                const uint32_t o = accSeq + (kPair ? (uint32_t)(yl >> 1) : (uint32_t)yl);
+                const uint32_t a = o % g.na, ka = o / g.na;
+                const uint32_t colq = kPair ? (uint32_t)(yl & 1) * g.nTpad : 0u;
                 const long long sI = cS[0] - cS[1] - cS[2] + cS[3];
                 const long long sI2 = cQ[0] - cQ[1] - cQ[2] + cQ[3];
                 if (yl + 1 < ty) load_corners(y + 1);  // next row's corners, in flight meanwhile
                 const long long vI = (long long)((unsigned long long)N * (unsigned)sI2) -
                                      (long long)((int)sI) * (long long)((int)sI);
-                const float rsI = vI > 0 ? rsqrtf(u64_to_f32((unsigned long long)vI)) : 0.f;
+                const float rsI = vI > 0 ? rsqrt_approx(u64_to_f32((unsigned long long)vI)) : 0.f;
                 const float sIf = (float)(int)sI;  // < 2^25: exact
-                mbar_wait_warp(&afull[a], ka & 1, &s_abort, p.status);
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (first) {
+                    mbar_wait_warp(&afull[a], ka & 1, &s_abort, p.status);
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                }
                 const size_t obase = (size_t)y * p.Ox + x;
                 if (kMoments && xin && ch == 0) {
                     p.sumI[obase] = sI;
@@ -422,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                 for (int ci = ch; ci * 32 < g.nTpad; ci += 2) {
                     const int cc = 32 * ci;
                     uint32_t v[32];
-                    tc_ld32(tmem + lane_base + a * g.accCols + cc, v);
+                    tc_ld32(tmem + lane_base + a * g.accCols + colq + cc, v);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                     if (!kOneGroup) {
                         // several exact groups: sum their integer values
@@ -437,6 +507,37 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                         }
                     }
                     if (!xin) continue;
+                    if constexpr (!kMoments && kOneGroup) {
+                        // r = (N*SumIT - SumI*SumT) / sqrt(vI*vT) with the numerator
+                        // exact up to its last rounding: p2 = fl(SumI*SumT), e2 its
+                        // exact error (fma), fma(N, SumIT, -p2) a single rounding of
+                        // N*SumIT - p2 (exact whenever it is small).  The output
+                        // pointer steps one template plane per coefficient.
+                        float *op = p.out + obase + (size_t)cc * plane;
+                        const float4 *st4 = reinterpret_cast<const float4 *>(sts + cc);
+                        auto run = [&](auto fullTag) {
+                            constexpr bool kFullChunk = decltype(fullTag)::value;
+                            const int nHere = p.nT - cc;
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2) {
+                                const float4 s2 = st4[i / 2];
+#pragma unroll
+                                for (int j = 0; j < 2; ++j) {
+                                    if (!kFullChunk && i + j >= nHere) continue;
+                                    const float sT = j ? s2.z : s2.x, rT = j ? s2.w : s2.y;
+                                    const float sit = __uint_as_float(v[i + j]);  // exact integer < 2^24
+                                    const float p2 = sIf * sT, e2 = fmaf(sIf, sT, -p2);
+                                    const float num = fmaf(Nf, sit, -p2) - e2;
+                                    float r = num * (rsI * rT);
+                                    r = fminf(1.0f, fmaxf(-1.0f, r));
+                                    __stcs(op, r);
+                                    op += plane;
+                                }
+                            }
+                        };
+                        if (cc + 32 <= p.nT) run(BoolTag<true>{});
+                        else run(BoolTag<false>{});
+                    } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
                         const int t = cc + i;
@@ -463,14 +564,17 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                         r = fminf(1.0f, fmaxf(-1.0f, r));
                         __stcs(p.out + oo, r);
                     }
+                    }
                 }
-                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&aempty[a]);
+                if (last) {
+                    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&aempty[a]);
+                }
             }
         }
         rowSeq += nrows;
-        outSeq += ty;
+        accSeq += kPair ? (uint32_t)((ty + 1) >> 1) : (uint32_t)ty;
     }
 
     // --- teardown: every accumulator has been drained by the epilogue ---
@@ -490,7 +594,7 @@ bool bank_tc_supported(int W, int H, int wT, int hT, int nT) {
     (void)W;
     (void)H;
     BankGeom g;
-    return nT >= 2 && make_geom(wT, hT, nT, g);
+    return nT >= 2 && (make_geom(wT, hT, nT, true, g) || make_geom(wT, hT, nT, false, g));
 }
 
 cudaError_t bank_tc_launch(const BankArgs &a, cudaStream_t stream) {
@@ -508,7 +612,8 @@ cudaError_t bank_tc_launch(const BankArgs &a, cudaStream_t stream) {
     p.Oy = a.H - a.hT + 1;
     p.ntx = (p.Ox + kM - 1) / kM;
     p.ntiles = p.ntx * ((p.Oy + kTY - 1) / kTY);
-    if (!make_geom(a.wT, a.hT, a.nT, p.g)) return cudaErrorNotSupported;
+    if (!make_geom(a.wT, a.hT, a.nT, true, p.g) && !make_geom(a.wT, a.hT, a.nT, false, p.g))
+        return cudaErrorNotSupported;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -519,20 +624,22 @@ cudaError_t bank_tc_launch(const BankArgs &a, cudaStream_t stream) {
     }
     const int grid = p.ntiles < 2 * g_num_sms[dev] ? p.ntiles : 2 * g_num_sms[dev];
     const size_t smem = (size_t)p.g.smemBytes;
-#define NCC_BANK(M, G1)                                                                          \
+#define NCC_BANK(M, G1, PR)                                                                   \
     do {                                                                                         \
-        e = cudaFuncSetAttribute(bank_tc_kernel<M, G1>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                 (int)smem);                                                     \
+        e = cudaFuncSetAttribute(bank_tc_kernel<M, G1, PR>,                                      \
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);        \
         if (e != cudaSuccess) return e;                                                          \
-        bank_tc_kernel<M, G1><<<grid, kThreads, smem, stream>>>(p);                              \
+        bank_tc_kernel<M, G1, PR><<<grid, kThreads, smem, stream>>>(p);                          \
     } while (0)
-    const bool one = p.g.nG == 1;
+    const bool one = p.g.nG == 1, pair = p.g.pair;
     if (a.sumIT) {
-        if (one) NCC_BANK(true, true);
-        else NCC_BANK(true, false);
+        if (pair) NCC_BANK(true, true, true);
+        else if (one) NCC_BANK(true, true, false);
+        else NCC_BANK(true, false, false);
     } else {
-        if (one) NCC_BANK(false, true);
-        else NCC_BANK(false, false);
+        if (pair) NCC_BANK(false, true, true);
+        else if (one) NCC_BANK(false, true, false);
+        else NCC_BANK(false, false, false);
     }
 #undef NCC_BANK
     return cudaGetLastError();
