@@ -443,7 +443,10 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
             }
             __syncwarp();
         } else {
-            // ---- epilogue: thread = shift x0 + 32*sp + lane, template chunks ci = ch (mod 2) ----
+            // ---- epilogue: thread = shift x0 + 32*sp + lane; the two warps of a
+            // lane quarter split the work: template chunks ci = ch (mod 2) of
+            // every row, or (pair mode) every chunk of row ch of each pair, so
+            // that no row's corners are loaded twice ----
             const int sp = warp & 3, ch = (warp - 4) >> 2;
             const int x = x0 + 32 * sp + lane;
             const uint32_t lane_base = (uint32_t)(32 * sp) << 16;
@@ -463,33 +466,33 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                 if (xl >= 0) { cS[2] = __ldg(p.S + (size_t)ybm * W + xl); cQ[2] = __ldg(p.Q + (size_t)ybm * W + xl); }
                 if (xl >= 0 && yt >= 0) { cS[3] = __ldg(p.S + (size_t)yt * W + xl); cQ[3] = __ldg(p.Q + (size_t)yt * W + xl); }
             };
-            load_corners(y0);
-            for (int yl = 0; yl < ty; ++yl) {
-                const int y = y0 + yl;
-                // pair mode: rows yl, yl+1 (yl even) share accumulator yl/2,
-                // row yl+1 in its second half of columns
-                const bool first = !kPair || (yl & 1) == 0;
-                const bool last = !kPair || (yl & 1) == 1 || yl + 1 == ty;
-                const uint32_t o = accSeq + (kPair ? (uint32_t)(yl >> 1) : (uint32_t)yl);
-                const uint32_t a = o % g.na, ka = o / g.na;
-                const uint32_t colq = kPair ? (uint32_t)(yl & 1) * g.nTpad : 0u;
+            // pair mode: rows yl = ch, ch+2, ... (accumulator yl/2, row ch of
+            // its two), all template chunks; otherwise every row, chunks ch, ch+2
+            const int rowStep = kPair ? 2 : 1, yFirst = kPair ? ch : 0;
+            const int ciStart = kPair ? 0 : ch, ciStep = kPair ? 1 : 2;
+            const int nIter = kPair ? (ty + 1) >> 1 : ty;
+            const uint32_t colq = kPair ? (uint32_t)ch * g.nTpad : 0u;
+            if (yFirst < ty) load_corners(y0 + yFirst);
+            for (int it = 0; it < nIter; ++it) {
+                const int yl = yFirst + it * rowStep, y = y0 + yl;
+                const bool valid = yl < ty;  // false only for row ch = 1 of a last single-row pair
+                const uint32_t o = accSeq + (uint32_t)it, a = o % g.na, ka = o / g.na;
                 const long long sI = cS[0] - cS[1] - cS[2] + cS[3];
                 const long long sI2 = cQ[0] - cQ[1] - cQ[2] + cQ[3];
-                if (yl + 1 < ty) load_corners(y + 1);  // next row's corners, in flight meanwhile
+                if (yl + rowStep < ty) load_corners(y + rowStep);  // next row's corners, in flight meanwhile
                 const long long vI = (long long)((unsigned long long)N * (unsigned)sI2) -
                                      (long long)((int)sI) * (long long)((int)sI);
                 const float rsI = vI > 0 ? rsqrt_approx(u64_to_f32((unsigned long long)vI)) : 0.f;
                 const float sIf = (float)(int)sI;  // < 2^25: exact
-                if (first) {
-                    mbar_wait_warp(&afull[a], ka & 1, &s_abort, p.status);
-                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                }
+                if (valid) {
+                mbar_wait_warp(&afull[a], ka & 1, &s_abort, p.status);
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const size_t obase = (size_t)y * p.Ox + x;
-                if (kMoments && xin && ch == 0) {
+                if (kMoments && xin && (kPair || ch == 0)) {
                     p.sumI[obase] = sI;
                     p.sumI2[obase] = sI2;
                 }
-                for (int ci = ch; ci * 32 < g.nTpad; ci += 2) {
+                for (int ci = ciStart; ci * 32 < g.nTpad; ci += ciStep) {
                     const int cc = 32 * ci;
                     uint32_t v[32];
                     tc_ld32(tmem + lane_base + a * g.accCols + colq + cc, v);
@@ -566,11 +569,10 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                     }
                     }
                 }
-                if (last) {
-                    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&aempty[a]);
                 }
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&aempty[a]);
             }
         }
         rowSeq += nrows;
