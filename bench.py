@@ -33,6 +33,9 @@ from normalized_cross_correlation_gb300 import inputs  # noqa: E402
 METRIC = "NCC coefficients/s (4096², 16×16 tmpl); SAT build GB/s vs HBM peak"
 UNIT = "coefficients/s"
 DEFAULT_WORKLOAD = "ncc_4096_t16"
+# summed-area-table builders (ncc_sat_build_variant): the fused single pass is
+# the product path; the naive and two-pass builds are the ones it is compared with
+SAT_VARIANTS = {"fused": 0, "naive": 1, "two_pass": 2}
 SAT_BYTES_PER_PX = 17          # 1 B read + 8 B (S) + 8 B (Q) written per pixel
 CORR_BYTES_PER_COEFF = 21      # S and Q corners (16 B after reuse) + 1 B image + 4 B out
 L2_FLUSH_BYTES = 512 << 20     # > 129 MB L2
@@ -221,8 +224,14 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     ev_mid = None
 
+    variant = SAT_VARIANTS[args.sat_variant]
+
     def step():
-        rc = L.ncc_sat_build(img.data_ptr(), w.W, w.H, S.data_ptr(), Q.data_ptr(), sh)
+        if variant == 0:
+            rc = L.ncc_sat_build(img.data_ptr(), w.W, w.H, S.data_ptr(), Q.data_ptr(), sh)
+        else:
+            rc = L.ncc_sat_build_variant(img.data_ptr(), w.W, w.H, S.data_ptr(), Q.data_ptr(),
+                                         variant, sh)
         assert rc == 0, rc
         if not nT:
             return
@@ -300,7 +309,7 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
     sat_gbs = SAT_BYTES_PER_PX * w.W * w.H / (sat_ms * 1e-3) / 1e9
     roof_sat = {"kernel": "sat_build", "bound": "hbm", "achieved": sat_gbs, "peak": hbm,
                 "unit": "GB/s", "frac": sat_gbs / hbm,
-                "traffic": NCU_TRAFFIC_BYTES.get(("sat_build", w.name)),
+                "traffic": NCU_TRAFFIC_BYTES.get(("sat_build", w.name)) if variant == 0 else None,
                 "peak_source": peaks["source"]}
     rooflines = [roof_sat]
     corr = None
@@ -354,6 +363,7 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
                    "templates": f"{nT}x{w.hT}x{w.wT} u8" if nT else None,
                    "step": "ncc_sat_build + " + ("ncc_correlate" if nT == 1 else
                                                  "ncc_correlate_bank" if nT else "nothing"),
+                   "sat_builder": args.sat_variant,
                    "l2": "flushed between timed steps (512 MB write)"},
         "sat_build": {"ms": sat_ms, "GB/s": sat_gbs, "frac_of_hbm": sat_gbs / hbm},
         "correlate": corr,
@@ -361,7 +371,7 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
         "rooflines": rooflines,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": (2 if nT else 1) * args.steps,
+        "gpu_launches": ((1 if nT else 0) + (1 if variant == 0 else 2)) * args.steps,
         "clocks": clocks.summary(),
     }
 
@@ -376,6 +386,9 @@ def main():
                     help="output rows of the oracle's bounded sample per step "
                          "(default: about 2e10 multiply-adds' worth)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--sat-variant", default="fused", choices=sorted(SAT_VARIANTS),
+                    help="summed-area-table builder: the single pass (default) or one of the "
+                         "builds it is compared with")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.NAMED),
                     help="workload to time (the default is the headline metric's)")
     args = ap.parse_args()

@@ -85,6 +85,29 @@ int ncc_sat_build(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
                   ncc_stream_t stream);
 
 /*
+ * ncc_sat_build_variant -- the same tables by one of the builders that
+ * section 15.8 compares (Figures 15-8 and 15-9), for measuring that
+ * comparison on this GPU.  variant:
+ *   NCC_SAT_FUSED     the single-pass tiled look-back of ncc_sat_build (the
+ *                     product path; this call is ncc_sat_build);
+ *   NCC_SAT_NAIVE     one thread per image row writes the rows' running sums
+ *                     into S and Q, then one thread per column adds down its
+ *                     column in place;
+ *   NCC_SAT_TWO_PASS  row running sums to a uint32 intermediate, then a
+ *                     column scan with a decoupled look-back over stripes of
+ *                     128 rows (no transposes).
+ *   Arguments, layouts and results as ncc_sat_build; NCC_ERR_INVALID_ARG for
+ *   an unknown variant.  The two-pass builder allocates (cudaMalloc) a
+ *   per-device workspace of 8 bytes per pixel plus its look-back words on
+ *   first use and when a larger image needs more; it is kept for later calls
+ *   and is not safe against concurrent calls on other streams.  Look-back
+ *   waits that run out record NCC_ERR_TIMEOUT for ncc_sync_status.
+ */
+enum ncc_sat_variant { NCC_SAT_FUSED = 0, NCC_SAT_NAIVE = 1, NCC_SAT_TWO_PASS = 2 };
+int ncc_sat_build_variant(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q, int variant,
+                          ncc_stream_t stream);
+
+/*
  * ncc_sat_build_noalloc -- ncc_sat_build for callers that cannot allocate
  * device memory (the pages have no counterpart: it is an interface
  * addition).  Callers inside a CUDA stream capture, a host callback, a

@@ -153,6 +153,28 @@ int ncc_sat_build(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int ncc_sat_build_variant(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q, int variant,
+                          ncc_stream_t stream) {
+    if (variant == NCC_SAT_FUSED) return ncc_sat_build(img, W, H, S, Q, stream);
+    if (variant != NCC_SAT_NAIVE && variant != NCC_SAT_TWO_PASS) return NCC_ERR_INVALID_ARG;
+    int rc = check_image(img, W, H);
+    if (rc != NCC_OK) return rc;
+    if (!S || !Q || (uintptr_t)S % 8 || (uintptr_t)Q % 8) return NCC_ERR_INVALID_ARG;
+    const size_t n = (size_t)W * H;
+    if (overlaps(S, n * 8, Q, n * 8) || overlaps(S, n * 8, img, n) || overlaps(Q, n * 8, img, n))
+        return NCC_ERR_INVALID_ARG;
+    int *status = nullptr;
+    rc = status_ptr(&status);
+    if (rc != NCC_OK) return rc;
+    uint64_t timeout;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        timeout = g_timeout_ns;
+    }
+    return to_status(ncc::sat_ladder_run(variant, img, W, H, S, Q, status, timeout,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int ncc_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT,
                   const int64_t *S, const int64_t *Q, float *out, ncc_stream_t stream) {
     return ncc_correlate_bank(img, W, H, tmpl, wT, hT, 1, S, Q, out, stream);

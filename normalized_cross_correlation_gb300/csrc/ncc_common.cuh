@@ -127,6 +127,10 @@ SatPlan sat_plan(int W, int H);
 cudaError_t sat_launch(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
                        void *workspace, const SatPlan &plan, uint32_t epoch, int *status,
                        uint64_t timeout_ns, int fault_tile, cudaStream_t stream);
+// The naive and two-pass builders of the SAT ladder (variant NCC_SAT_NAIVE
+// or NCC_SAT_TWO_PASS), on their own per-device workspace.
+cudaError_t sat_ladder_run(int variant, const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
+                           int *status, uint64_t timeout_ns, cudaStream_t stream);
 // The builder on the library's per-device workspace (allocated on first use).
 cudaError_t sat_build_run(const uint8_t *img, int W, int H, int64_t *S, int64_t *Q,
                           int *status, uint64_t timeout_ns, int fault_tile,

@@ -22,7 +22,11 @@ NCC_ERR_CUDA = -3
 NCC_ERR_TIMEOUT = -4
 NCC_ERR_NOMEM = -5
 
-EXPORTS = ("ncc_sat_build", "ncc_sat_build_noalloc", "ncc_correlate", "ncc_correlate_bank", "ncc_correlate_moments",
+NCC_SAT_FUSED = 0      # the single-pass tiled look-back (ncc_sat_build)
+NCC_SAT_NAIVE = 1      # one thread per row, then one thread per column
+NCC_SAT_TWO_PASS = 2   # uint32 row sums, then a column look-back scan
+
+EXPORTS = ("ncc_sat_build", "ncc_sat_build_noalloc", "ncc_sat_build_variant", "ncc_correlate", "ncc_correlate_bank", "ncc_correlate_moments",
            "ncc_match_host", "ncc_sync_status", "ncc_status_string", "ncc_version",
            "ncc_debug_set_fault", "ncc_debug_set_path", "ncc_debug_last_path")
 
@@ -54,6 +58,7 @@ def lib() -> ctypes.CDLL:
             vp, i, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64
             L.ncc_sat_build.argtypes = [vp, i, i, vp, vp, vp]
             L.ncc_sat_build_noalloc.argtypes = [vp, i, i, vp, vp, vp]
+            L.ncc_sat_build_variant.argtypes = [vp, i, i, vp, vp, i, vp]
             L.ncc_correlate.argtypes = [vp, i, i, vp, i, i, vp, vp, vp, vp]
             L.ncc_correlate_bank.argtypes = [vp, i, i, vp, i, i, i, vp, vp, vp, vp]
             L.ncc_correlate_moments.argtypes = [vp, i, i, vp, i, i, i, vp, vp, vp, vp, vp, vp]
@@ -121,6 +126,23 @@ def ncc_sat_build(img, S=None, Q=None, stream=None):
     _dev(Q, torch.int64, 2, "Q")
     _check(lib().ncc_sat_build(img.data_ptr(), W, H, S.data_ptr(), Q.data_ptr(),
                                _stream_handle(stream)), "ncc_sat_build")
+    return S, Q
+
+
+def ncc_sat_build_variant(img, variant, S=None, Q=None, stream=None):
+    """The same tables by one of the compared builders (NCC_SAT_FUSED,
+    NCC_SAT_NAIVE, NCC_SAT_TWO_PASS)."""
+    import torch
+    _dev(img, torch.uint8, 2, "img")
+    H, W = img.shape
+    if S is None:
+        S = torch.empty((H, W), dtype=torch.int64, device=img.device)
+    if Q is None:
+        Q = torch.empty((H, W), dtype=torch.int64, device=img.device)
+    _dev(S, torch.int64, 2, "S")
+    _dev(Q, torch.int64, 2, "Q")
+    _check(lib().ncc_sat_build_variant(img.data_ptr(), W, H, S.data_ptr(), Q.data_ptr(), int(variant),
+                                       _stream_handle(stream)), "ncc_sat_build_variant")
     return S, Q
 
 
