@@ -62,6 +62,12 @@ constexpr int kMaxSmem = 227 * 1024;   // opt-in shared memory per CTA
 constexpr int kEpiStages = 2;          // table-row staging ring depth
 constexpr int kEpiRowsPerStep = 4;     // output rows per epilogue step (rows per TMA box)
 constexpr int kEpiBufs = 4;            // boxes per stage: S top, S bottom, Q top, Q bottom
+// Templates at most kNarrowT wide share one table-row segment width, so the
+// kernel instantiated for them addresses the staged rows with immediate
+// offsets.
+constexpr int kNarrowT = 16;
+constexpr int kNarrowBW = (kOutW + kNarrowT + 2) & ~1;                        // 146 columns
+constexpr int kNarrowBuf = (kEpiRowsPerStep * kNarrowBW * 8 + 127) / 128 * 128;  // bytes per box
 // Templates of at most this many pixels form the coefficient's numerator
 // N*SumIT - SumI*SumT and variance term N*SumI2 - SumI^2 in 32-bit integers:
 // both are N^2 times a covariance or variance of values in 0..255, so at
@@ -88,6 +94,7 @@ Geom make_geom(int wT, int hT) {
     const int sumBytes = kOutH * kOutW * 4;  // the SumIT transpose reuses the tile's space
     g.tmplOff = tileBytes > sumBytes ? tileBytes : sumBytes;
     g.epiBW = (kOutW + wT + 2) & ~1;   // columns x0-2 .. x0+wT+127, rounded up to even
+    if (wT <= kNarrowT) g.epiBW = kNarrowBW;  // one fixed layout for narrow templates
     g.epiBuf = (kEpiRowsPerStep * g.epiBW * 8 + 127) / 128 * 128;
     g.epiOff = (g.tmplOff + hT * g.nch * 16 + 127) / 128 * 128;
     g.smemBytes = g.epiOff + kEpiStages * kEpiBufs * g.epiBuf + 128;
@@ -173,7 +180,8 @@ __device__ __forceinline__ void mbar_wait(unsigned long long *bar, uint32_t pari
     }
 }
 
-template <bool kTma, bool kMoments, bool kTmaEpi>
+// kNarrow: the template is at most kNarrowT wide (fixed staged layout).
+template <bool kTma, bool kMoments, bool kTmaEpi, bool kNarrow>
 __global__ void __launch_bounds__(kThreads, 3)
 corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmS,
                  const __grid_constant__ CUtensorMap tmQ, const KParams p) {
@@ -188,6 +196,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     __shared__ float s_invSqrtVT;
 
     const Geom &g = p.g;
+    const int epiBW = kNarrow ? kNarrowBW : g.epiBW, epiBuf = kNarrow ? kNarrowBuf : g.epiBuf;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int x0 = blockIdx.x * kOutW, y0 = blockIdx.y * kOutH;
     const int epiSteps = (min(kOutH, p.Oy - y0) + kEpiRowsPerStep - 1) / kEpiRowsPerStep;
@@ -199,13 +208,13 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         const int y = y0 + kEpiRowsPerStep * t;  // first output row of the step
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                      ::"r"(smem_u32(&s_ebar[st])),
-                       "r"((uint32_t)(kEpiBufs * kEpiRowsPerStep * g.epiBW * 8))
+                       "r"((uint32_t)(kEpiBufs * kEpiRowsPerStep * epiBW * 8))
                      : "memory");
-        uint8_t *b = epi + st * kEpiBufs * g.epiBuf;
+        uint8_t *b = epi + st * kEpiBufs * epiBuf;
         tma_2d(&tmS, b, x0 - 2, y - 1, &s_ebar[st]);                      // rows y-1 ..
-        tma_2d(&tmS, b + g.epiBuf, x0 - 2, y + p.hT - 1, &s_ebar[st]);    // rows y+hT-1 ..
-        tma_2d(&tmQ, b + 2 * g.epiBuf, x0 - 2, y - 1, &s_ebar[st]);
-        tma_2d(&tmQ, b + 3 * g.epiBuf, x0 - 2, y + p.hT - 1, &s_ebar[st]);
+        tma_2d(&tmS, b + epiBuf, x0 - 2, y + p.hT - 1, &s_ebar[st]);      // rows y+hT-1 ..
+        tma_2d(&tmQ, b + 2 * epiBuf, x0 - 2, y - 1, &s_ebar[st]);
+        tma_2d(&tmQ, b + 3 * epiBuf, x0 - 2, y + p.hT - 1, &s_ebar[st]);
     };
 
     if (kTmaEpi && tid == 0) {
@@ -379,7 +388,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     const bool smallN = N <= kMaxInt32N;
     const uint32_t Nu = (uint32_t)N, sTu = (uint32_t)sT;
     const int h = warp >> 2, xo = (warp & 3) * 32 + lane, x = x0 + xo;
-    const int segWords = g.epiBW * 2;                          // u32 words per table-row segment
+    const int segWords = epiBW * 2;                            // u32 words per table-row segment
     const int cl = 2 * (xo + 1), cr = 2 * (xo + p.wT + 1);      // low words of x-1, x+wT-1
     // the loop is instantiated per coefficient path and for full tiles
     // (every output row and column valid: no per-output bounds checks)
@@ -395,8 +404,8 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
             uint32_t done = 0;
             if (lane == 0) done = mbar_try(&s_ebar[st], par);
             if (!__shfl_sync(0xffffffffu, done, 0)) mbar_wait(&s_ebar[st], par, p.status);
-            const uint32_t *b = reinterpret_cast<const uint32_t *>(epi + st * kEpiBufs * g.epiBuf);
-            const int box = g.epiBuf / 4;                          // u32 words per box
+            const uint32_t *b = reinterpret_cast<const uint32_t *>(epi + st * kEpiBufs * epiBuf);
+            const int box = epiBuf / 4;                            // u32 words per box
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 const int o = (h + 2 * q) * segWords;
@@ -537,17 +546,20 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
     const dim3 block(kThreads);
     const size_t smem = (size_t)p.g.smemBytes;
     cudaError_t e;
-#define NCC_LAUNCH(T, M, E)                                                                  \
+#define NCC_LAUNCH(T, M, E, NW)                                                              \
     do {                                                                                     \
-        e = cudaFuncSetAttribute(corr_dp4a_kernel<T, M, E>,                                  \
+        e = cudaFuncSetAttribute(corr_dp4a_kernel<T, M, E, NW>,                              \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);    \
         if (e != cudaSuccess) return e;                                                      \
-        corr_dp4a_kernel<T, M, E><<<grid, block, smem, stream>>>(tmap, tmS, tmQ, p);         \
+        corr_dp4a_kernel<T, M, E, NW><<<grid, block, smem, stream>>>(tmap, tmS, tmQ, p);     \
     } while (0)
-#define NCC_LAUNCH_E(T, M)                    \
-    do {                                      \
-        if (tmaEpi) NCC_LAUNCH(T, M, true);   \
-        else NCC_LAUNCH(T, M, false);         \
+    // the fixed narrow layout only where the rows are staged by TMA
+    const bool narrow = a.wT <= kNarrowT;
+#define NCC_LAUNCH_E(T, M)                                      \
+    do {                                                        \
+        if (tmaEpi && narrow) NCC_LAUNCH(T, M, true, true);     \
+        else if (tmaEpi) NCC_LAUNCH(T, M, true, false);         \
+        else NCC_LAUNCH(T, M, false, false);                    \
     } while (0)
     if (tma && moments) NCC_LAUNCH_E(true, true);
     else if (tma) NCC_LAUNCH_E(true, false);
