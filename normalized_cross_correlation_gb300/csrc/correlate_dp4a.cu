@@ -458,11 +458,10 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                     vIpos = vI > 0;
                     vIf = vIpos ? u64_to_f32((unsigned long long)vI) : 1.f;
                 }
-                float r = 0.0f;
-                if (vIpos && vT > 0) {
-                    r = num * rsqrt_approx(vIf) * invSqrtVT;
-                    r = fminf(1.0f, fmaxf(-1.0f, r));
-                }
+                // invSqrtVT is 0 for a zero-variance template; vIf >= 1
+                // whenever vIpos, so the product is finite where it is kept
+                const float rr = num * rsqrt_approx(vIf) * invSqrtVT;
+                const float r = vIpos ? fminf(1.0f, fmaxf(-1.0f, rr)) : 0.0f;
                 __stcs(p.out + o, r);
             }
         }
