@@ -67,6 +67,12 @@ def test_argument_checks_need_no_gpu(built_lib):
     assert L.ncc_correlate(fake, 16, 16, fake * 2, 4, 4, fake * 8, fake * 16, fake * 8,
                            None) == ncc.NCC_ERR_INVALID_ARG
     assert L.ncc_match_host(None, 16, 16, fake, 4, 4, 1, fake, None) == ncc.NCC_ERR_INVALID_ARG
+    # the compared SAT builders: unknown variant, then the same checks as ncc_sat_build
+    assert L.ncc_sat_build_variant(fake, 16, 16, fake * 4, fake * 8, 9, None) == ncc.NCC_ERR_INVALID_ARG
+    for v in (ncc.NCC_SAT_FUSED, ncc.NCC_SAT_NAIVE, ncc.NCC_SAT_TWO_PASS):
+        assert L.ncc_sat_build_variant(fake, 0, 16, fake * 4, fake * 8, v, None) == ncc.NCC_ERR_INVALID_ARG
+        assert L.ncc_sat_build_variant(fake, 66052, 1, fake * 4, fake * 8, v, None) == ncc.NCC_ERR_UNSUPPORTED
+        assert L.ncc_sat_build_variant(fake, 16, 16, fake * 4, fake * 4 + 8, v, None) == ncc.NCC_ERR_INVALID_ARG
     assert L.ncc_debug_set_fault(-2, 0) == ncc.NCC_ERR_INVALID_ARG
 
 
