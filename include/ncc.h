@@ -119,7 +119,7 @@ int ncc_sat_build_variant(const uint8_t *img, int W, int H, int64_t *S, int64_t 
  * holds until the process exits.
  *   Arguments, layouts, results and errors as ncc_sat_build, plus:
  *   NCC_ERR_UNSUPPORTED when the image needs more scratch than 8 MiB, i.e.
- *   when ceil(W/128) * ceil(H/128) > 2730 tiles (4096x4096 fits; 8192x8192
+ *   when ceil(W/128) * ceil(H/128) > 2729 tiles (4096x4096 fits; 8192x8192
  *   does not).
  * The first call on a device looks up the scratch array's device address
  * (cudaGetSymbolAddress); make it before any stream capture.  All calls on
