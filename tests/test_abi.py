@@ -67,6 +67,10 @@ def test_argument_checks_need_no_gpu(built_lib):
     assert L.ncc_correlate(fake, 16, 16, fake * 2, 4, 4, fake * 8, fake * 16, fake * 8,
                            None) == ncc.NCC_ERR_INVALID_ARG
     assert L.ncc_match_host(None, 16, 16, fake, 4, 4, 1, fake, None) == ncc.NCC_ERR_INVALID_ARG
+    # the no-alloc builder's fixed scratch holds at most 2729 tiles of 128x128:
+    # 42 x 65 = 2730 tiles is refused before any device work
+    assert L.ncc_sat_build_noalloc(fake, 128 * 42, 128 * 65, 1 << 32, (1 << 32) + (1 << 30),
+                                   None) == ncc.NCC_ERR_UNSUPPORTED
     # the compared SAT builders: unknown variant, then the same checks as ncc_sat_build
     assert L.ncc_sat_build_variant(fake, 16, 16, fake * 4, fake * 8, 9, None) == ncc.NCC_ERR_INVALID_ARG
     for v in (ncc.NCC_SAT_FUSED, ncc.NCC_SAT_NAIVE, ncc.NCC_SAT_TWO_PASS):
