@@ -181,7 +181,8 @@ __device__ __forceinline__ void mbar_wait(unsigned long long *bar, uint32_t pari
 }
 
 // kNarrow: the template is at most kNarrowT wide (fixed staged layout).
-template <bool kTma, bool kMoments, bool kTmaEpi, bool kNarrow>
+// kHT: the template height when fixed at compile time (0: run time).
+template <bool kTma, bool kMoments, bool kTmaEpi, bool kNarrow, int kHT>
 __global__ void __launch_bounds__(kThreads, 3)
 corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmS,
                  const __grid_constant__ CUtensorMap tmQ, const KParams p) {
@@ -225,7 +226,6 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         }
         asm volatile("fence.mbarrier_init.release.cluster;");
         asm volatile("fence.proxy.async.shared::cta;");
-        for (int t = 0; t < kEpiStages && t < epiSteps; ++t) issue_epi(t);
     }
 
     // --- stage the image tile (copy 0) ---------------------------------
@@ -243,7 +243,12 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                 ::"r"(smem_u32(smem)), "l"(&tmap), "r"(x0), "r"(y0), "r"(smem_u32(&s_bar))
                 : "memory");
         }
-    } else {
+    }
+    // The first table-row stages are requested after the image tile: this
+    // SM's copies are served in order, and the tile is needed first.
+    if (kTmaEpi && tid == 0)
+        for (int t = 0; t < kEpiStages && t < epiSteps; ++t) issue_epi(t);
+    if (!kTma) {
         for (int idx = tid; idx < g.boxW * g.boxH; idx += kThreads) {
             const int r = idx / g.boxW, c = idx - r * g.boxW;
             const int y = y0 + r, x = x0 + c;
@@ -294,6 +299,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     // Lane 4*qg + d reads 32 aligned bytes at 16*qg (+16 per chunk) and
     // moves them by d bytes with one byte permute per word, so each of its
     // shifts x0 + 16*qg + 4*k + d sees 32-bit groups of four pixels.
+    const int hT = kHT ? kHT : p.hT;
     const int qg = lane >> 2, d = lane & 3;
     const uint32_t sel = 0x3210u + 0x1111u * (uint32_t)d;
     const uint8_t *cp = smem + 16 * qg;
@@ -305,7 +311,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
 
     for (int c = 0; c < g.nch; ++c) {
         const uint8_t *cc = cp + 16 * c + warp * kRowsPerThread * g.boxW;
-        const uint4 *tc = reinterpret_cast<const uint4 *>(tw) + c * p.hT;  // chunk c of row j at tc[j]
+        const uint4 *tc = reinterpret_cast<const uint4 *>(tw) + c * hT;  // chunk c of row j at tc[j]
         // the d-shifted words of tile row r of this warp
         auto row_words = [&](int r, uint32_t (&v)[7]) {
             const uint8_t *rp = cc + r * g.boxW;
@@ -328,7 +334,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                 a[k] = s;
             }
         };
-        if (p.hT >= kRowsPerThread) {
+        if (hT >= kRowsPerThread) {
             // tile row r meets output rows i = max(0, r-hT+1) .. min(7, r):
             // ramp-up rows, full rows and ramp-down rows, without branches
 #pragma unroll
@@ -338,29 +344,37 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
 #pragma unroll
                 for (int i = 0; i <= r; ++i) mac(acc[i], v, tc[r - i]);
             }
-            for (int r = kRowsPerThread - 1; r < p.hT; ++r) {
+            auto full_row = [&](int r) {
                 uint32_t v[7];
                 row_words(r, v);
 #pragma unroll
                 for (int i = 0; i < kRowsPerThread; ++i) mac(acc[i], v, tc[r - i]);
+            };
+            if constexpr (kHT != 0) {
+                // fixed height: the phase unrolls and the template rows it
+                // reads stay in registers from one tile row to the next
+#pragma unroll
+                for (int r = kRowsPerThread - 1; r < kHT; ++r) full_row(r);
+            } else {
+                for (int r = kRowsPerThread - 1; r < hT; ++r) full_row(r);
             }
 #pragma unroll
             for (int m = 0; m < kRowsPerThread - 1; ++m) {
-                const int r = p.hT + m;
+                const int r = hT + m;
                 uint32_t v[7];
                 row_words(r, v);
 #pragma unroll
                 for (int i = m + 1; i < kRowsPerThread; ++i) mac(acc[i], v, tc[r - i]);
             }
         } else {
-            const int rows = kRowsPerThread + p.hT - 1;
+            const int rows = kRowsPerThread + hT - 1;
             for (int r = 0; r < rows; ++r) {
                 uint32_t v[7];
                 row_words(r, v);
 #pragma unroll
                 for (int i = 0; i < kRowsPerThread; ++i) {
                     const int j = r - i;
-                    if (j >= 0 && j < p.hT) mac(acc[i], v, tc[j]);
+                    if (j >= 0 && j < hT) mac(acc[i], v, tc[j]);
                 }
             }
         }
@@ -368,12 +382,20 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
 
     // --- transpose SumIT through shared memory ------------------------------
     __syncthreads();  // every warp is done with the staged copies
-    uint32_t *sIT = reinterpret_cast<uint32_t *>(smem);  // [kOutH][kOutW]
+    // [kOutH][kOutW], column c stored at c ^ (((c >> 5) & 3) << 2): the
+    // 32 lanes of one store (columns 16*qg + 4*k + d) then fall in 32
+    // different banks, and a row read of 32 consecutive columns still does.
+    uint32_t *sIT = reinterpret_cast<uint32_t *>(smem);
+    {
+        uint32_t *sw = sIT + 16 * qg + d;
 #pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i)
+        for (int k = 0; k < 4; ++k) {
+            const int ck = 4 * (k ^ (qg >> 1));
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            sIT[(warp * kRowsPerThread + i) * kOutW + 16 * qg + 4 * k + d] = acc[i][k];
+            for (int i = 0; i < kRowsPerThread; ++i)
+                sw[(warp * kRowsPerThread + i) * kOutW + ck] = acc[i][k];
+        }
+    }
     __syncthreads();
 
     // --- epilogue: moments from S and Q, coefficient -----------------------
@@ -388,6 +410,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     const bool smallN = N <= kMaxInt32N;
     const uint32_t Nu = (uint32_t)N, sTu = (uint32_t)sT;
     const int h = warp >> 2, xo = (warp & 3) * 32 + lane, x = x0 + xo;
+    const int xs = xo ^ ((warp & 3) << 2);                     // column xo in the SumIT layout
     const int segWords = epiBW * 2;                            // u32 words per table-row segment
     const int cl = 2 * (xo + 1), cr = 2 * (xo + p.wT + 1);      // low words of x-1, x+wT-1
     // the loop is instantiated per coefficient path and for full tiles
@@ -432,7 +455,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
             if (x > 0 && y > 0) { sI += (uint32_t)__ldg(St + xl); sI2 += (uint32_t)__ldg(Qt + xl); }
         }
         if (kFull || (y < p.Oy && x < p.Ox)) {
-            const unsigned sumIT = sIT[row * kOutW + xo];
+            const unsigned sumIT = sIT[row * kOutW + xs];
             const size_t o = (size_t)y * p.Ox + x;
             if (kMoments) {
                 p.sumI[o] = (long long)sI;
@@ -545,20 +568,22 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
     const dim3 block(kThreads);
     const size_t smem = (size_t)p.g.smemBytes;
     cudaError_t e;
-#define NCC_LAUNCH(T, M, E, NW)                                                              \
+#define NCC_LAUNCH(T, M, E, NW, HT)                                                          \
     do {                                                                                     \
-        e = cudaFuncSetAttribute(corr_dp4a_kernel<T, M, E, NW>,                              \
+        e = cudaFuncSetAttribute(corr_dp4a_kernel<T, M, E, NW, HT>,                          \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);    \
         if (e != cudaSuccess) return e;                                                      \
-        corr_dp4a_kernel<T, M, E, NW><<<grid, block, smem, stream>>>(tmap, tmS, tmQ, p);     \
+        corr_dp4a_kernel<T, M, E, NW, HT><<<grid, block, smem, stream>>>(tmap, tmS, tmQ, p); \
     } while (0)
-    // the fixed narrow layout only where the rows are staged by TMA
+    // the fixed narrow layout only where the rows are staged by TMA; a
+    // compile-time height for the common 16-row templates on that path
     const bool narrow = a.wT <= kNarrowT;
-#define NCC_LAUNCH_E(T, M)                                      \
-    do {                                                        \
-        if (tmaEpi && narrow) NCC_LAUNCH(T, M, true, true);     \
-        else if (tmaEpi) NCC_LAUNCH(T, M, true, false);         \
-        else NCC_LAUNCH(T, M, false, false);                    \
+#define NCC_LAUNCH_E(T, M)                                                  \
+    do {                                                                    \
+        if (tmaEpi && narrow && a.hT == 16) NCC_LAUNCH(T, M, true, true, 16); \
+        else if (tmaEpi && narrow) NCC_LAUNCH(T, M, true, true, 0);         \
+        else if (tmaEpi) NCC_LAUNCH(T, M, true, false, 0);                  \
+        else NCC_LAUNCH(T, M, false, false, 0);                             \
     } while (0)
     if (tma && moments) NCC_LAUNCH_E(true, true);
     else if (tma) NCC_LAUNCH_E(true, false);

@@ -44,6 +44,8 @@ CASES = [  # (W, H, wT, hT)
     (64, 64, 64, 64), (1000, 260, 13, 31), (272, 96, 100, 40), (513, 70, 128, 20),
     # grouped table-row loads: partial last block of 4*hT rows, views shifted by H mod hT
     (512, 300, 12, 7), (256, 157, 8, 15), (320, 133, 20, 2),
+    # 16-row templates on the TMA path (compile-time height), ragged last tiles
+    (528, 200, 16, 16), (256, 100, 5, 16), (1024, 131, 16, 16),
 ]
 
 
