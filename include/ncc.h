@@ -175,9 +175,27 @@ int ncc_correlate_moments(const uint8_t *img, int W, int H,
                           int64_t *sumI2, int64_t *sumIT, ncc_stream_t stream);
 
 /*
+ * ncc_match -- the whole path on device buffers: ncc_sat_build(img) into S
+ * and Q, then ncc_correlate_bank of the nT templates against them, ordered
+ * on `stream` (the SAT serves the denominators and the templates' numerators
+ * follow, as in section 15.8).  For a single template the correlation kernel
+ * is launched with programmatic stream serialization: its CTAs may start as
+ * the SAT build's CTAs retire and run their numerators (which read only img
+ * and tmpl), and they wait for the build to finish before they read S or Q.
+ * The results are those of the two separate calls, bit for bit.
+ *   S, Q device int64 [H][W], written (caller-owned, as ncc_sat_build);
+ *   other arguments as ncc_correlate_bank.  S and Q must not overlap img,
+ *   tmpl, out or each other.
+ * Returns as ncc_correlate_bank.
+ */
+int ncc_match(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
+              int hT, int nT, int64_t *S, int64_t *Q, float *out,
+              ncc_stream_t stream);
+
+/*
  * ncc_match_host -- the whole path with HOST buffers: copies img and tmpl to
- * the device, builds S and Q, correlates every template and copies the
- * coefficients back, all ordered on `stream`, then synchronizes it.
+ * the device, runs ncc_match on them and copies the coefficients back, all
+ * ordered on `stream`, then synchronizes it.
  *   img  host uint8 [H][W];  tmpl host uint8 [nT][hT][wT];
  *   out  host fp32 [nT][Oy][Ox].  Page-locked host memory makes the copies
  *   asynchronous and fast; pageable memory also works.

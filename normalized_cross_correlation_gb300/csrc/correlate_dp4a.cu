@@ -56,6 +56,7 @@ constexpr int kRowsPerThread = 8;
 constexpr int kWarps = 8;
 constexpr int kOutH = kWarps * kRowsPerThread;  // 64
 constexpr int kThreads = kWarps * 32;
+constexpr int kMaxCtasPerSm = 3;   // resident CTAs per SM (launch bound)
 constexpr int kMaxTmaBox = 256;        // TMA box extent limit per dimension
 constexpr int kMaxSmem = 227 * 1024;   // opt-in shared memory per CTA
 
@@ -111,6 +112,7 @@ struct KParams {
     long long *sumI, *sumI2, *sumIT;
     int *status;
     int Ox, Oy;
+    int lateWave;    // CTAs (linear id) that request their first table rows after the numerator
     Geom g;
 };
 
@@ -153,6 +155,12 @@ __device__ __forceinline__ void tma_2d(const CUtensorMap *map, void *dst, int x,
         : "memory");
 }
 
+// Waits until the grid this kernel depends on programmatically has finished
+// and its writes are visible; returns at once for an ordinary launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t mbar_try(unsigned long long *bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
@@ -183,7 +191,7 @@ __device__ __forceinline__ void mbar_wait(unsigned long long *bar, uint32_t pari
 // kNarrow: the template is at most kNarrowT wide (fixed staged layout).
 // kHT: the template height when fixed at compile time (0: run time).
 template <bool kTma, bool kMoments, bool kTmaEpi, bool kNarrow, int kHT>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, kMaxCtasPerSm)
 corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmS,
                  const __grid_constant__ CUtensorMap tmQ, const KParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -245,9 +253,14 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         }
     }
     // The first table-row stages are requested after the image tile: this
-    // SM's copies are served in order, and the tile is needed first.
-    if (kTmaEpi && tid == 0)
+    // SM's copies are served in order, and the tile is needed first.  The
+    // CTAs of the first wave of an overlapped launch may start before the
+    // tables are complete: they request them after their numerator.
+    const bool lateIssue = (int)(blockIdx.y * gridDim.x + blockIdx.x) < p.lateWave;
+    if (kTmaEpi && tid == 0 && !lateIssue) {
+        grid_dependency_wait();
         for (int t = 0; t < kEpiStages && t < epiSteps; ++t) issue_epi(t);
+    }
     if (!kTma) {
         for (int idx = tid; idx < g.boxW * g.boxH; idx += kThreads) {
             const int r = idx / g.boxW, c = idx - r * g.boxW;
@@ -380,6 +393,11 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         }
     }
 
+    if (kTmaEpi && tid == 0 && lateIssue) {
+        grid_dependency_wait();
+        for (int t = 0; t < kEpiStages && t < epiSteps; ++t) issue_epi(t);
+    }
+
     // --- transpose SumIT through shared memory ------------------------------
     __syncthreads();  // every warp is done with the staged copies
     // [kOutH][kOutW], column c stored at c ^ (((c >> 5) & 3) << 2): the
@@ -405,6 +423,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     // terms are exact 32-bit integers; larger templates take exact 64-bit
     // integers.
     const long long N = (long long)p.wT * p.hT;
+    grid_dependency_wait();  // S and Q are complete (the plain-load epilogue reads them)
     const long long sT = s_sumT, vT = s_vT;
     const float invSqrtVT = s_invSqrtVT;
     const bool smallN = N <= kMaxInt32N;
@@ -519,6 +538,7 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
     p.sumIT = reinterpret_cast<long long *>(a.sumIT);
     p.status = a.status;
     p.Ox = a.W - a.wT + 1;
+    p.lateWave = a.overlap_prev ? kMaxCtasPerSm * sm_count() : 0;
     p.Oy = a.H - a.hT + 1;
     p.g = make_geom(a.wT, a.hT);
 
@@ -573,7 +593,22 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
         e = cudaFuncSetAttribute(corr_dp4a_kernel<T, M, E, NW, HT>,                          \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);    \
         if (e != cudaSuccess) return e;                                                      \
-        corr_dp4a_kernel<T, M, E, NW, HT><<<grid, block, smem, stream>>>(tmap, tmS, tmQ, p); \
+        if (a.overlap_prev) {                                                                \
+            cudaLaunchConfig_t cfg = {};                                                     \
+            cfg.gridDim = grid;                                                              \
+            cfg.blockDim = block;                                                            \
+            cfg.dynamicSmemBytes = smem;                                                     \
+            cfg.stream = stream;                                                             \
+            cudaLaunchAttribute attr[1];                                                     \
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;                 \
+            attr[0].val.programmaticStreamSerializationAllowed = 1;                          \
+            cfg.attrs = attr;                                                                \
+            cfg.numAttrs = 1;                                                                \
+            e = cudaLaunchKernelEx(&cfg, corr_dp4a_kernel<T, M, E, NW, HT>, tmap, tmS, tmQ, p); \
+            if (e != cudaSuccess) return e;                                                  \
+        } else {                                                                             \
+            corr_dp4a_kernel<T, M, E, NW, HT><<<grid, block, smem, stream>>>(tmap, tmS, tmQ, p); \
+        }                                                                                    \
     } while (0)
     // the fixed narrow layout only where the rows are staged by TMA; a
     // compile-time height for the common 16-row templates on that path

@@ -68,9 +68,11 @@ int to_status(cudaError_t e) {
 }
 
 // Numerator + epilogue for nT templates, either coefficients or moments.
+// after_sat: the previous kernel on the stream is this library's SAT build
+// of img, so a single-template launch may overlap its tail.
 int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT, int nT,
                   const int64_t *S, const int64_t *Q, float *out, int64_t *sumI,
-                  int64_t *sumI2, int64_t *sumIT, cudaStream_t stream) {
+                  int64_t *sumI2, int64_t *sumIT, cudaStream_t stream, bool after_sat = false) {
     int *status = nullptr;
     int rc = status_ptr(&status);
     if (rc != NCC_OK) return rc;
@@ -101,12 +103,13 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
         a.sumI2 = sumI2;
         a.sumIT = sumIT ? sumIT + (size_t)t * plane : nullptr;
         a.status = status;
+        a.overlap_prev = after_sat && t == 0;
         cudaError_t e = cudaErrorNotSupported;
         // Automatic selection takes the dp4a kernel: on the 4096x4096 /
         // 16x16 workload it measures faster than the tensor-core kernel
         // (about 200 vs 250 us), whose tiny N = 16 MMAs leave it bound by
         // pipeline hand-off latency rather than by the tensor pipe.
-        if (path == NCC_PATH_TENSOR && ncc::corr_tc_supported(a)) {
+        if (path == NCC_PATH_TENSOR && !a.overlap_prev && ncc::corr_tc_supported(a)) {
             e = ncc::corr_tc_launch(a, stream);
             if (e == cudaSuccess) used = NCC_PATH_TENSOR;
         }
@@ -211,6 +214,29 @@ int ncc_correlate_moments(const uint8_t *img, int W, int H, const uint8_t *tmpl,
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+int ncc_match(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT, int nT,
+              int64_t *S, int64_t *Q, float *out, ncc_stream_t stream) {
+    int rc = check_correlate(img, W, H, tmpl, wT, hT, nT, S, Q);
+    if (rc != NCC_OK) return rc;
+    if (!out || (uintptr_t)out % 4) return NCC_ERR_INVALID_ARG;
+    const size_t n = (size_t)W * H;
+    const size_t nout = (size_t)nT * (W - wT + 1) * (H - hT + 1) * sizeof(float);
+    if (overlaps(out, nout, S, n * 8) || overlaps(out, nout, Q, n * 8) ||
+        overlaps(out, nout, img, n) || overlaps(out, nout, tmpl, (size_t)nT * wT * hT) ||
+        overlaps(S, n * 8, tmpl, (size_t)nT * wT * hT) || overlaps(Q, n * 8, tmpl, (size_t)nT * wT * hT))
+        return NCC_ERR_INVALID_ARG;
+    rc = ncc_sat_build(img, W, H, S, Q, stream);   // checks S, Q against img and each other
+    if (rc != NCC_OK) return rc;
+    int path;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        path = g_path;
+    }
+    // the overlap only behind the fused builder, which lets its dependents start
+    return run_correlate(img, W, H, tmpl, wT, hT, nT, S, Q, out, nullptr, nullptr, nullptr,
+                         reinterpret_cast<cudaStream_t>(stream), path != NCC_PATH_TENSOR);
+}
+
 int ncc_match_host(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT,
                    int nT, float *out, ncc_stream_t stream) {
     int rc = check_image(img, W, H);
@@ -233,8 +259,7 @@ int ncc_match_host(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT
     if (cudaMemcpyAsync(dimg, img, n, cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemcpyAsync(dt, tmpl, nt, cudaMemcpyHostToDevice, st) != cudaSuccess)
         rc = NCC_ERR_CUDA;
-    if (rc == NCC_OK) rc = ncc_sat_build(dimg, W, H, S, Q, stream);
-    if (rc == NCC_OK) rc = ncc_correlate_bank(dimg, W, H, dt, wT, hT, nT, S, Q, dout, stream);
+    if (rc == NCC_OK) rc = ncc_match(dimg, W, H, dt, wT, hT, nT, S, Q, dout, stream);
     if (rc == NCC_OK &&
         cudaMemcpyAsync(out, dout, nout * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         rc = NCC_ERR_CUDA;

@@ -146,7 +146,15 @@ struct CorrArgs {
     float *out;                 // coefficients (null when moments are requested)
     int64_t *sumI, *sumI2, *sumIT;  // moments (all null unless requested)
     int *status;                // per-device status word
+    // Launch with programmatic stream serialization: the kernel may start
+    // while the previous kernel on the stream (the SAT build, which lets its
+    // dependents start) is still running; it reads only img and tmpl before
+    // it waits on that grid, and S and Q after.  Only for a previous kernel
+    // that writes neither img nor tmpl.
+    bool overlap_prev = false;
 };
+// Multiprocessors of the current device (cached per device).
+int sm_count();
 bool corr_dp4a_supported(int wT, int hT);
 cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream);
 // The same on the tensor cores (tcgen05; hT <= 16, wT*hT <= 258, wT <= 126,

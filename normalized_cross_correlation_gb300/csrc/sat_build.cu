@@ -311,6 +311,10 @@ sat_build_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__rest
     __shared__ unsigned s_tile, s_next;
     __shared__ int s_fail, s_last;
 
+    // A kernel launched after this one with programmatic serialization may
+    // be scheduled as this grid's CTAs retire (it waits on this grid before
+    // it reads the tables).
+    asm volatile("griddepcontrol.launch_dependents;");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (warp < kGroups) {
         // ================= producer warps: tiles, scans, look-backs =================

@@ -27,7 +27,7 @@ NCC_SAT_NAIVE = 1      # one thread per row, then one thread per column
 NCC_SAT_TWO_PASS = 2   # uint32 row sums, then a column look-back scan
 
 EXPORTS = ("ncc_sat_build", "ncc_sat_build_noalloc", "ncc_sat_build_variant", "ncc_correlate", "ncc_correlate_bank", "ncc_correlate_moments",
-           "ncc_match_host", "ncc_sync_status", "ncc_status_string", "ncc_version",
+           "ncc_match", "ncc_match_host", "ncc_sync_status", "ncc_status_string", "ncc_version",
            "ncc_debug_set_fault", "ncc_debug_set_path", "ncc_debug_last_path")
 
 _lock = threading.Lock()
@@ -62,6 +62,7 @@ def lib() -> ctypes.CDLL:
             L.ncc_correlate.argtypes = [vp, i, i, vp, i, i, vp, vp, vp, vp]
             L.ncc_correlate_bank.argtypes = [vp, i, i, vp, i, i, i, vp, vp, vp, vp]
             L.ncc_correlate_moments.argtypes = [vp, i, i, vp, i, i, i, vp, vp, vp, vp, vp, vp]
+            L.ncc_match.argtypes = [vp, i, i, vp, i, i, i, vp, vp, vp, vp]
             L.ncc_match_host.argtypes = [vp, i, i, vp, i, i, i, vp, vp]
             L.ncc_sync_status.argtypes = [vp]
             L.ncc_status_string.argtypes = [i]
@@ -211,6 +212,31 @@ def ncc_correlate_moments(img, tmpls, S, Q, stream=None):
                                        sI2.data_ptr(), sIT.data_ptr(), _stream_handle(stream)),
            "ncc_correlate_moments")
     return sI, sI2, sIT
+
+
+def ncc_match(img, tmpls, S=None, Q=None, out=None, stream=None):
+    """SAT build then correlation on device tensors, in one call: returns
+    (S, Q, out), with out fp32 [nT][Oy][Ox] (the single-template correlation
+    overlaps the build's tail)."""
+    import torch
+    _dev(img, torch.uint8, 2, "img")
+    tmpls = _tmpl3(tmpls)
+    _dev(tmpls, torch.uint8, 3, "tmpls")
+    H, W = img.shape
+    nT, hT, wT = tmpls.shape
+    if S is None:
+        S = torch.empty((H, W), dtype=torch.int64, device=img.device)
+    if Q is None:
+        Q = torch.empty((H, W), dtype=torch.int64, device=img.device)
+    _dev(S, torch.int64, 2, "S")
+    _dev(Q, torch.int64, 2, "Q")
+    if out is None:
+        out = torch.empty((nT, max(H - hT + 1, 0), max(W - wT + 1, 0)), dtype=torch.float32,
+                          device=img.device)
+    _dev(out, torch.float32, 3, "out")
+    _check(lib().ncc_match(img.data_ptr(), W, H, tmpls.data_ptr(), wT, hT, nT, S.data_ptr(),
+                           Q.data_ptr(), out.data_ptr(), _stream_handle(stream)), "ncc_match")
+    return S, Q, out
 
 
 def ncc_match_host(img, tmpls, out=None, stream=None):

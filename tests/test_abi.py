@@ -18,7 +18,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("ncc_sat_build", "ncc_correlate", "ncc_correlate_bank", "ncc_sync_status",
-                 "ncc_status_string", "ncc_correlate_moments", "ncc_match_host"):
+                 "ncc_status_string", "ncc_correlate_moments", "ncc_match", "ncc_match_host"):
         assert want in names
 
 
@@ -67,6 +67,15 @@ def test_argument_checks_need_no_gpu(built_lib):
     assert L.ncc_correlate(fake, 16, 16, fake * 2, 4, 4, fake * 8, fake * 16, fake * 8,
                            None) == ncc.NCC_ERR_INVALID_ARG
     assert L.ncc_match_host(None, 16, 16, fake, 4, 4, 1, fake, None) == ncc.NCC_ERR_INVALID_ARG
+    # the combined call: missing image, overlapping tables, a table over the templates
+    assert L.ncc_match(None, 16, 16, fake * 2, 4, 4, 1, fake * 8, fake * 16, fake * 32,
+                       None) == ncc.NCC_ERR_INVALID_ARG
+    assert L.ncc_match(fake, 16, 16, fake * 2, 4, 4, 1, fake * 8, fake * 8 + 8, fake * 32,
+                       None) == ncc.NCC_ERR_INVALID_ARG
+    assert L.ncc_match(fake, 16, 16, fake * 8 + 16, 4, 4, 1, fake * 8, fake * 16, fake * 32,
+                       None) == ncc.NCC_ERR_INVALID_ARG
+    assert L.ncc_match(fake, 16, 16, fake * 2, 4, 4, 1, fake * 8, fake * 16, fake * 8 + 64,
+                       None) == ncc.NCC_ERR_INVALID_ARG
     # the no-alloc builder's fixed scratch holds at most 2729 tiles of 128x128:
     # 42 x 65 = 2730 tiles is refused before any device work
     assert L.ncc_sat_build_noalloc(fake, 128 * 42, 128 * 65, 1 << 32, (1 << 32) + (1 << 30),

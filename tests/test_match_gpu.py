@@ -1,0 +1,102 @@
+"""GPU parity of ncc_match, the combined call (SAT build, then the
+correlation, whose single-template launch overlaps the build's tail).
+
+Its tables and coefficients must equal, bit for bit, those of the separate
+ncc_sat_build + ncc_correlate(_bank) calls (which the other GPU tests hold to
+the oracle), and on small cases the oracle directly: tables bit-exact,
+coefficients within 1e-5 absolute.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from normalized_cross_correlation_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+
+
+def to_dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def separate(ncc, dimg, dt):
+    S, Q = ncc.ncc_sat_build(dimg)
+    if dt.dim() == 3 and dt.shape[0] > 1:
+        out = ncc.ncc_correlate_bank(dimg, dt, S, Q)
+    else:
+        out = ncc.ncc_correlate(dimg, dt.reshape(dt.shape[-2:]), S, Q).unsqueeze(0)
+    assert ncc.ncc_sync_status() == 0
+    return S.cpu().numpy(), Q.cpu().numpy(), out.cpu().numpy()
+
+
+# (W, H, wT, hT, nT): TMA paths with the fixed 16-row kernel, the plain-load
+# paths (odd width), other heights, a bank, ragged last tiles
+SHAPES = [
+    (1024, 768, 16, 16, 1), (523, 300, 7, 5, 1), (2048, 1100, 8, 8, 1), (1000, 260, 13, 31, 1),
+    (640, 480, 16, 16, 4), (272, 200, 16, 16, 1),
+]
+
+
+@pytest.mark.parametrize("W,H,wT,hT,nT", SHAPES)
+def test_match_equals_separate_calls(ncc, W, H, wT, hT, nT):
+    w = inputs.random_case(W * 7 + H * 3 + nT, W, H, wT, hT, nT=nT, n_crops=1)
+    dimg, dt = to_dev(w.image), to_dev(w.templates)
+    S0, Q0, r0 = separate(ncc, dimg, dt)
+    S, Q, r = ncc.ncc_match(dimg, dt)
+    assert ncc.ncc_sync_status() == 0
+    np.testing.assert_array_equal(S.cpu().numpy(), S0)
+    np.testing.assert_array_equal(Q.cpu().numpy(), Q0)
+    np.testing.assert_array_equal(r.cpu().numpy(), r0)
+
+
+def test_match_small_case_matches_oracle(ncc, threads):
+    w = inputs.random_case(4242, 300, 200, 16, 16, nT=1, n_crops=1)
+    S, Q, r = ncc.ncc_match(to_dev(w.image), to_dev(w.templates))
+    assert ncc.ncc_sync_status() == 0
+    oS, oQ = oracle.sat(w.image)
+    np.testing.assert_array_equal(S.cpu().numpy(), oS)
+    np.testing.assert_array_equal(Q.cpu().numpy(), oQ)
+    ref = oracle.correlate(w.image, w.templates[0], threads=threads)
+    np.testing.assert_allclose(r.cpu().numpy()[0], ref, rtol=0, atol=TOL)
+
+
+def test_headline_size_on_a_side_stream_repeatedly(ncc):
+    """The bench's configuration (4096x4096, one 16x16 template), five calls
+    in a row on a non-default stream, interleaved with the separate calls:
+    every result is the same."""
+    import torch
+    w = inputs.headline_4096()
+    dimg, dt = to_dev(w.image), to_dev(w.templates)
+    _, _, r0 = separate(ncc, dimg, dt)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        S = torch.empty((w.H, w.W), dtype=torch.int64, device="cuda")
+        Q = torch.empty_like(S)
+        out = torch.empty((1, w.Oy, w.Ox), dtype=torch.float32, device="cuda")
+        for _ in range(5):
+            out.fill_(7.0)
+            ncc.ncc_match(dimg, dt, S, Q, out, stream=s)
+            assert ncc.ncc_sync_status(s) == 0
+            np.testing.assert_array_equal(out.cpu().numpy(), r0)
+            ncc.ncc_correlate(dimg, dt[0], S, Q, out[0], stream=s)
+            assert ncc.ncc_sync_status(s) == 0
+            np.testing.assert_array_equal(out.cpu().numpy(), r0)
+
+
+def test_match_on_the_tensor_path_takes_no_overlap(ncc):
+    """With the tensor-core single-template kernel selected (it has no grid
+    dependency wait), ncc_match launches it in plain stream order."""
+    w = inputs.random_case(99, 512, 256, 16, 16, nT=1, n_crops=1)
+    dimg, dt = to_dev(w.image), to_dev(w.templates)
+    _, _, r0 = separate(ncc, dimg, dt)
+    ncc.ncc_debug_set_path(ncc.NCC_PATH_TENSOR)
+    try:
+        S, Q, r = ncc.ncc_match(dimg, dt)
+        assert ncc.ncc_sync_status() == 0
+        assert ncc.ncc_debug_last_path() == ncc.NCC_PATH_TENSOR
+    finally:
+        ncc.ncc_debug_set_path(0)
+    np.testing.assert_allclose(r.cpu().numpy(), r0, rtol=0, atol=TOL)
