@@ -194,14 +194,18 @@ int ncc_match(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
 
 /*
  * ncc_match_host -- the whole path with HOST buffers: copies img and tmpl to
- * the device, runs ncc_match on them and copies the coefficients back, all
+ * the device, runs ncc_match on them and brings the coefficients back, all
  * ordered on `stream`, then synchronizes it.
  *   img  host uint8 [H][W];  tmpl host uint8 [nT][hT][wT];
  *   out  host fp32 [nT][Oy][Ox].  Page-locked host memory makes the copies
- *   asynchronous and fast; pageable memory also works.
- * Device buffers come from cudaMallocAsync on `stream` and are released
- * before return.  Returns the first failure among the steps, including any
- * status recorded by the kernels (as ncc_sync_status would).
+ *   asynchronous and fast; pageable memory also works.  When `out` is
+ *   page-locked memory the device can address, the kernels store the
+ *   coefficients into it directly; otherwise they go to a device buffer that
+ *   is copied back.
+ * Device buffers come from a stream-ordered pool that the library keeps per
+ * device (memory freed to it stays reserved for the next call) and go back
+ * to it before return.  Returns the first failure among the steps, including
+ * any status recorded by the kernels (as ncc_sync_status would).
  */
 int ncc_match_host(const uint8_t *img, int W, int H, const uint8_t *tmpl,
                    int wT, int hT, int nT, float *out, ncc_stream_t stream);

@@ -61,6 +61,35 @@ int check_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int w
     return NCC_OK;
 }
 
+// Stream-ordered pool for the host-buffer path's device buffers, one per
+// device.  Its release threshold keeps freed memory reserved, so repeated
+// calls reuse it instead of mapping it afresh after every synchronization
+// (what the default pool, which releases at each synchronization, would do).
+cudaMemPool_t g_host_pool[kMaxDevices] = {};
+
+int host_path_pool(cudaMemPool_t *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NCC_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_host_pool[dev]) {
+        cudaMemPoolProps props;
+        memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return NCC_ERR_CUDA;
+        uint64_t keep = ~0ull;
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return NCC_ERR_CUDA;
+        }
+        g_host_pool[dev] = pool;
+    }
+    *out = g_host_pool[dev];
+    return NCC_OK;
+}
+
 int to_status(cudaError_t e) {
     if (e == cudaSuccess) return NCC_OK;
     if (e == cudaErrorMemoryAllocation) return NCC_ERR_NOMEM;
@@ -246,21 +275,38 @@ int ncc_match_host(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const size_t n = (size_t)W * H, nt = (size_t)nT * wT * hT;
     const size_t nout = (size_t)nT * (W - wT + 1) * (H - hT + 1);
+    // Page-locked output the device can address: the kernels store the
+    // coefficients straight into it over the host link, so there is no
+    // separate device-to-host copy after them.  Otherwise a device buffer
+    // and one copy.
+    float *direct = nullptr;
+    {
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, out) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+            pa.devicePointer && (uintptr_t)pa.devicePointer % 4 == 0)
+            direct = static_cast<float *>(pa.devicePointer);
+        else
+            (void)cudaGetLastError();  // pageable memory: clear the query's error, if any
+    }
     // one device block: tables first (8-byte aligned), then out, image, templates
-    const size_t offQ = n * 8, offOut = 2 * n * 8, offImg = (offOut + nout * 4 + 255) / 256 * 256;
+    const size_t outBytes = direct ? 0 : nout * 4;
+    const size_t offQ = n * 8, offOut = 2 * n * 8, offImg = (offOut + outBytes + 255) / 256 * 256;
     const size_t offT = (offImg + n + 255) / 256 * 256, total = offT + nt;
+    cudaMemPool_t pool = nullptr;
+    rc = host_path_pool(&pool);
+    if (rc != NCC_OK) return rc;
     char *d = nullptr;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&d), total, st);
+    cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&d), total, pool, st);
     if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? NCC_ERR_NOMEM : NCC_ERR_CUDA;
     int64_t *S = reinterpret_cast<int64_t *>(d), *Q = reinterpret_cast<int64_t *>(d + offQ);
-    float *dout = reinterpret_cast<float *>(d + offOut);
+    float *dout = direct ? direct : reinterpret_cast<float *>(d + offOut);
     uint8_t *dimg = reinterpret_cast<uint8_t *>(d + offImg), *dt = reinterpret_cast<uint8_t *>(d + offT);
     rc = NCC_OK;
     if (cudaMemcpyAsync(dimg, img, n, cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemcpyAsync(dt, tmpl, nt, cudaMemcpyHostToDevice, st) != cudaSuccess)
         rc = NCC_ERR_CUDA;
     if (rc == NCC_OK) rc = ncc_match(dimg, W, H, dt, wT, hT, nT, S, Q, dout, stream);
-    if (rc == NCC_OK &&
+    if (rc == NCC_OK && !direct &&
         cudaMemcpyAsync(out, dout, nout * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         rc = NCC_ERR_CUDA;
     cudaFreeAsync(d, st);

@@ -100,3 +100,23 @@ def test_match_on_the_tensor_path_takes_no_overlap(ncc):
     finally:
         ncc.ncc_debug_set_path(0)
     np.testing.assert_allclose(r.cpu().numpy(), r0, rtol=0, atol=TOL)
+
+
+@pytest.mark.parametrize("W,H,wT,hT,nT,pinned", [
+    (1024, 600, 16, 16, 1, True), (1024, 600, 16, 16, 1, False),
+    (523, 300, 7, 5, 1, True), (640, 480, 16, 16, 4, True), (640, 480, 16, 16, 4, False),
+])
+def test_host_entry_point_matches_device_path(ncc, W, H, wT, hT, nT, pinned):
+    """ncc_match_host with page-locked output (the kernels store into it
+    directly) and with pageable output (a device buffer and a copy back)."""
+    import torch
+    w = inputs.random_case(W + 5 * H + nT, W, H, wT, hT, nT=nT, n_crops=1)
+    _, _, r0 = separate(ncc, to_dev(w.image), to_dev(w.templates))
+    img, T = torch.from_numpy(w.image), torch.from_numpy(w.templates)
+    out = torch.full((nT, w.Oy, w.Ox), 7.0, dtype=torch.float32)
+    if pinned:
+        img, T, out = img.pin_memory(), T.pin_memory(), out.pin_memory()
+    for _ in range(2):                        # the second call reuses the pooled buffers
+        out.fill_(7.0)
+        ncc.ncc_match_host(img, T, out)
+        np.testing.assert_array_equal(out.numpy(), r0)
