@@ -413,6 +413,96 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
     }
 
 
+def run_gpu_direct(args, w: inputs.Workload) -> dict | None:
+    """The direct-moment correlation (ncc_correlate_direct): one kernel per
+    template and step, no summed-area tables.  A comparison line, not the
+    headline: the method's denominators come from the tables."""
+    import torch
+    from normalized_cross_correlation_gb300 import ncc
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    L = ncc.lib()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    dev = torch.device("cuda", local)
+    nT = w.nT
+    img = torch.from_numpy(w.image).to(dev)
+    tmpl = torch.from_numpy(w.templates).to(dev)
+    out = torch.empty((nT, w.Oy, w.Ox), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        rc = L.ncc_correlate_direct(img.data_ptr(), w.W, w.H, tmpl.data_ptr(), w.wT, w.hT, nT,
+                                    out.data_ptr(), sh)
+        assert rc == 0, rc
+
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert ncc.ncc_sync_status() == 0
+    clocks = ClockSampler(local)
+    with clocks:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for k in range(args.steps):
+            flush.zero_()                       # L2 flushed between timed steps
+            ev_a[k].record(stream)
+            step()
+            ev_b[k].record(stream)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+    assert ncc.ncc_sync_status() == 0
+    t = [ev_a[k].elapsed_time(ev_b[k]) for k in range(args.steps)]
+    ms = max_over_ranks(statistics.mean(t), dist, dev)
+    coeffs = nT * w.Ox * w.Oy
+    value = job_rate(coeffs, ws, ms)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    dp4a = coeffs * ((w.wT + 3) // 4) * w.hT
+    alu_peak = DP4A_PER_SM_CLK * N_SMS * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+    corr_bytes = 4 * coeffs + w.W * w.H * nT      # coefficients out, the image once per template
+    r_alu = {"kernel": "corr_dp4a_direct", "bound": "alu", "achieved": dp4a / (ms * 1e-3) / 1e12,
+             "peak": alu_peak / 1e12, "unit": "Tdp4a/s", "frac": dp4a / (ms * 1e-3) / alu_peak,
+             "traffic": None}
+    gbs = corr_bytes / (ms * 1e-3) / 1e9
+    r_hbm = {"kernel": "corr_dp4a_direct", "bound": "hbm", "achieved": gbs, "peak": hbm,
+             "unit": "GB/s", "frac": gbs / hbm, "traffic": None}
+    dominant = max(r_alu, r_hbm, key=lambda r: r["frac"])
+    return {
+        "metric": f"NCC coefficients/s ({w.name}, direct moments)", "value": value, "unit": UNIT,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic",
+        "config": {"workload": w.name, "image": f"{w.W}x{w.H} u8",
+                   "templates": f"{nT}x{w.hT}x{w.wT} u8", "step": "ncc_correlate_direct",
+                   "moments": "direct (staged image tile, no summed-area tables)",
+                   "l2": "flushed between timed steps (512 MB write)"},
+        "correlate": {"kernel": "corr_dp4a_direct", "ms": ms, "GB/s": gbs,
+                      "GMAC/s": coeffs * w.wT * w.hT / (ms * 1e-3) / 1e9},
+        "roofline": {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")},
+        "rooflines": [r_alu, r_hbm],
+        "cpu_baseline": None,
+        "e2e": None,
+        "gpu_launches": nT * args.steps,
+        "clocks": clocks.summary(),
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -428,6 +518,9 @@ def main():
                          "builds it is compared with")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.NAMED),
                     help="workload to time (the default is the headline metric's)")
+    ap.add_argument("--moments", default="sat", choices=["sat", "direct"],
+                    help="window moments from the summed-area tables (the method, default) or "
+                         "from the staged image tile (ncc_correlate_direct, a comparison line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "gb300" else args.warmup
 
@@ -438,7 +531,9 @@ def main():
             return
         print(json.dumps(run_reference(args, w)), flush=True)
         return
-    res = run_gpu(args, w)
+    if args.moments == "direct" and not w.nT:
+        return
+    res = run_gpu_direct(args, w) if args.moments == "direct" else run_gpu(args, w)
     if res is not None:
         print(json.dumps(res), flush=True)
 

@@ -175,6 +175,33 @@ int ncc_correlate_moments(const uint8_t *img, int W, int H,
                           int64_t *sumI2, int64_t *sumIT, ncc_stream_t stream);
 
 /*
+ * ncc_correlate_direct -- the coefficients of nT templates without summed-area
+ * tables: the window moments SumI and SumI2 come from the image tile the
+ * numerator stages in shared memory, as the shared-memory kernel of chapter
+ * 15 (Listing 15-5) forms its window sums from the staged image.  Per pass of
+ * 16 output rows: sliding sums of I and I^2 down each tile column over hT
+ * rows, then exclusive prefix sums along each row; a window's sum is the
+ * difference of two prefixes (exact in wrapping 32-bit arithmetic).
+ *   img, tmpl, out, sizes and stream as ncc_correlate_bank; no S or Q.
+ *   wT <= 129.  Each template is one launch of the single-template kernel.
+ * The integer moments and the arithmetic are those of ncc_correlate, so for
+ * one template the coefficients equal ncc_correlate's bit for bit.
+ * Returns as ncc_correlate; NCC_ERR_UNSUPPORTED for wT > 129.
+ */
+int ncc_correlate_direct(const uint8_t *img, int W, int H, const uint8_t *tmpl,
+                         int wT, int hT, int nT, float *out, ncc_stream_t stream);
+
+/*
+ * ncc_correlate_direct_moments -- the exact integer sums behind
+ * ncc_correlate_direct, for verification: sumI, sumI2 device int64
+ * [Oy][Ox] and sumIT device int64 [nT][Oy][Ox], as ncc_correlate_moments.
+ */
+int ncc_correlate_direct_moments(const uint8_t *img, int W, int H,
+                                 const uint8_t *tmpl, int wT, int hT, int nT,
+                                 int64_t *sumI, int64_t *sumI2, int64_t *sumIT,
+                                 ncc_stream_t stream);
+
+/*
  * ncc_match -- the whole path on device buffers: ncc_sat_build(img) into S
  * and Q, then ncc_correlate_bank of the nT templates against them, ordered
  * on `stream` (the SAT serves the denominators and the templates' numerators

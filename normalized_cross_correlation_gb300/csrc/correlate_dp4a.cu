@@ -74,6 +74,11 @@ constexpr int kNarrowBuf = (kEpiRowsPerStep * kNarrowBW * 8 + 127) / 128 * 128; 
 // both are N^2 times a covariance or variance of values in 0..255, so at
 // most N^2 * 127.5^2 < 2^31 in magnitude.
 constexpr long long kMaxInt32N = 363;
+// Direct moments: output rows per pass of the column-sum / row-prefix
+// buffers (two tables of kDirRows rows in shared memory at a time).
+constexpr int kDirRows = 16;
+// Direct moments: tile columns one thread per column covers.
+constexpr int kDirMaxCols = kThreads;
 
 struct Geom {
     int nch;         // 16-pixel template chunks
@@ -83,16 +88,33 @@ struct Geom {
     int epiBW;       // table-row segment length (int64 elements), even
     int epiBuf;      // bytes per box (kEpiRowsPerStep table-row segments, 128-aligned)
     int epiOff;      // offset of the staging ring
+    int sumOff;      // offset of the SumIT transpose (0: over the dead tile)
+    int cpOff;       // direct moments: offset of the column-sum / row-prefix buffers
+    int cPitch;      // direct moments: u32 words per buffer row (odd, > kOutW + wT - 1)
     int smemBytes;   // dynamic shared memory (plus 128 bytes of alignment slack)
 };
 
-Geom make_geom(int wT, int hT) {
+// direct: the window moments come from the staged tile (the tile outlives
+// the numerator, so the SumIT transpose gets its own space) instead of from
+// the summed-area tables.
+Geom make_geom(int wT, int hT, bool direct = false) {
     Geom g;
     g.nch = (wT + 15) / 16;
     g.boxW = kOutW + 16 * g.nch;
     g.boxH = kOutH + hT - 1;
     const int tileBytes = (g.boxW * g.boxH + 127) / 128 * 128;
     const int sumBytes = kOutH * kOutW * 4;  // the SumIT transpose reuses the tile's space
+    if (direct) {
+        g.tmplOff = tileBytes;
+        g.sumOff = (g.tmplOff + hT * g.nch * 16 + 127) / 128 * 128;
+        g.cpOff = g.sumOff + sumBytes;
+        g.cPitch = (kOutW + wT) | 1;
+        g.epiBW = g.epiBuf = 0;
+        g.epiOff = g.cpOff;
+        g.smemBytes = g.cpOff + 2 * kDirRows * g.cPitch * 4 + 128;
+        return g;
+    }
+    g.sumOff = g.cpOff = g.cPitch = 0;
     g.tmplOff = tileBytes > sumBytes ? tileBytes : sumBytes;
     g.epiBW = (kOutW + wT + 2) & ~1;   // columns x0-2 .. x0+wT+127, rounded up to even
     if (wT <= kNarrowT) g.epiBW = kNarrowBW;  // one fixed layout for narrow templates
@@ -190,7 +212,8 @@ __device__ __forceinline__ void mbar_wait(unsigned long long *bar, uint32_t pari
 
 // kNarrow: the template is at most kNarrowT wide (fixed staged layout).
 // kHT: the template height when fixed at compile time (0: run time).
-template <bool kTma, bool kMoments, bool kTmaEpi, bool kNarrow, int kHT>
+// kDirect: window moments from the staged tile, not from S and Q.
+template <bool kTma, bool kMoments, bool kTmaEpi, bool kNarrow, int kHT, bool kDirect>
 __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm)
 corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmS,
                  const __grid_constant__ CUtensorMap tmQ, const KParams p) {
@@ -256,8 +279,10 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     // SM's copies are served in order, and the tile is needed first.  The
     // CTAs of the first wave of an overlapped launch may start before the
     // tables are complete: they request them after their numerator.
-    const bool lateIssue = (int)(blockIdx.y * gridDim.x + blockIdx.x) < p.lateWave;
-    if (kTmaEpi && tid == 0 && !lateIssue) {
+    // (recomputed where used: a flag kept live across the numerator costs a
+    // register the numerator needs)
+    auto late_issue = [&]() { return (int)(blockIdx.y * gridDim.x + blockIdx.x) < p.lateWave; };
+    if (kTmaEpi && tid == 0 && !late_issue()) {
         grid_dependency_wait();
         for (int t = 0; t < kEpiStages && t < epiSteps; ++t) issue_epi(t);
     }
@@ -393,7 +418,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         }
     }
 
-    if (kTmaEpi && tid == 0 && lateIssue) {
+    if (kTmaEpi && tid == 0 && late_issue()) {
         grid_dependency_wait();
         for (int t = 0; t < kEpiStages && t < epiSteps; ++t) issue_epi(t);
     }
@@ -403,7 +428,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     // [kOutH][kOutW], column c stored at c ^ (((c >> 5) & 3) << 2): the
     // 32 lanes of one store (columns 16*qg + 4*k + d) then fall in 32
     // different banks, and a row read of 32 consecutive columns still does.
-    uint32_t *sIT = reinterpret_cast<uint32_t *>(smem);
+    uint32_t *sIT = reinterpret_cast<uint32_t *>(smem + (kDirect ? g.sumOff : 0));
     {
         uint32_t *sw = sIT + 16 * qg + d;
 #pragma unroll
@@ -423,7 +448,9 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     // terms are exact 32-bit integers; larger templates take exact 64-bit
     // integers.
     const long long N = (long long)p.wT * p.hT;
-    grid_dependency_wait();  // S and Q are complete (the plain-load epilogue reads them)
+    // S and Q are complete: the plain-load epilogue reads them in every
+    // thread (with TMA only thread 0's requests do, after its own wait)
+    if constexpr (!kTmaEpi && !kDirect) grid_dependency_wait();
     const long long sT = s_sumT, vT = s_vT;
     const float invSqrtVT = s_invSqrtVT;
     const bool smallN = N <= kMaxInt32N;
@@ -514,16 +541,132 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         }
     }
     };
+    // Direct moments.  Per pass of kDirRows output rows: (1) thread t keeps
+    // the sums of I and I^2 over hT tile rows of tile column t, sliding down
+    // one row at a time, and stores them; (2) each stored row is replaced by
+    // its exclusive prefix over the columns; (3) SumI of the window at
+    // column c is prefix[c + wT] - prefix[c], and the same for SumI2.  The
+    // u32 arithmetic wraps, which is exact: both sums are below 2^32.
+    auto direct_epilogue = [&](auto smallTag, auto fullTag) {
+    constexpr bool kSmall = decltype(smallTag)::value, kFull = decltype(fullTag)::value;
+    const int ncols = kOutW + p.wT - 1;         // tile columns the windows cover
+    const int cP = g.cPitch;
+    uint32_t *P1 = reinterpret_cast<uint32_t *>(smem + g.cpOff), *P2 = P1 + kDirRows * cP;
+    const uint8_t *col = smem + tid;              // this thread's tile column
+    const bool colOwner = tid < ncols;
+    uint32_t c1 = 0, c2 = 0;
+    if (colOwner)
+        for (int j = 0; j < p.hT; ++j) {
+            const uint32_t v = col[j * g.boxW];
+            c1 += v;
+            c2 += v * v;
+        }
+    const int rowsValid = min(kOutH, p.Oy - y0);
+    const int per = (ncols + 31) >> 5;            // columns per lane in the prefix pass (<= 8)
+    for (int yb = 0; yb < rowsValid; yb += kDirRows) {
+        // (1) column sums of the pass's rows
+        if (colOwner) {
+#pragma unroll 4
+            for (int r = 0; r < kDirRows; ++r) {
+                const int yr = yb + r;
+                P1[r * cP + tid] = c1;
+                P2[r * cP + tid] = c2;
+                if (yr + 1 < kOutH) {                 // the tile holds rows 0 .. kOutH + hT - 2
+                    const uint32_t a = col[(yr + p.hT) * g.boxW], b = col[yr * g.boxW];
+                    c1 += a - b;
+                    c2 += a * a - b * b;
+                }
+            }
+        }
+        __syncthreads();
+        // (2) exclusive prefix of every stored row, in place: entry e holds
+        //     the sum of columns 0 .. e-1 (entry ncols the whole row)
+        for (int task = warp; task < 2 * kDirRows; task += kWarps) {
+            uint32_t *rowp = (task < kDirRows ? P1 : P2) + (task % kDirRows) * cP;
+            uint32_t s[8];
+            uint32_t run = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int c = lane * per + j;
+                run += (j < per && c < ncols) ? rowp[c] : 0u;
+                s[j] = run;
+            }
+            uint32_t incl = run;                      // inclusive scan of the lane totals
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += u;
+            }
+            const uint32_t base = incl - run;
+            __syncwarp();                             // every lane has read its columns
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int c = lane * per + j;
+                if (j < per && c < ncols) rowp[c + 1] = base + s[j];
+            }
+            if (lane == 0) rowp[0] = 0u;
+        }
+        __syncthreads();
+        // (3) coefficients of the pass's rows: thread = column xo, rows h, h+2, ..
+#pragma unroll 2
+        for (int i = 0; i < kDirRows / 2; ++i) {
+            const int r = h + 2 * i, row = yb + r, y = y0 + row;
+            if (kFull || (y < p.Oy && x < p.Ox)) {
+                const uint32_t sI = P1[r * cP + xo + p.wT] - P1[r * cP + xo];
+                const uint32_t sI2 = P2[r * cP + xo + p.wT] - P2[r * cP + xo];
+                const unsigned sumIT = sIT[row * kOutW + xs];
+                const size_t o = (size_t)y * p.Ox + x;
+                if (kMoments) {
+                    p.sumI[o] = (long long)sI;
+                    p.sumI2[o] = (long long)sI2;
+                    p.sumIT[o] = (long long)sumIT;
+                } else {
+                    float num, vIf;
+                    bool vIpos;
+                    if (kSmall) {
+                        num = (float)(int)(Nu * sumIT - sI * sTu);
+                        const uint32_t vIu = Nu * sI2 - sI * sI;
+                        vIpos = vIu != 0u;
+                        vIf = (float)vIu;
+                    } else {
+                        const long long numi = (long long)((unsigned long long)N * sumIT) -
+                                               (long long)sI * (long long)sT;
+                        const long long vI = (long long)((unsigned long long)N * sI2) -
+                                             (long long)sI * (long long)sI;
+                        num = i64_to_f32(numi);
+                        vIpos = vI > 0;
+                        vIf = vIpos ? u64_to_f32((unsigned long long)vI) : 1.f;
+                    }
+                    const float rr = num * rsqrt_approx(vIf) * invSqrtVT;
+                    const float rc = vIpos ? fminf(1.0f, fmaxf(-1.0f, rr)) : 0.0f;
+                    __stcs(p.out + o, rc);
+                }
+            }
+        }
+        __syncthreads();                              // before the next pass overwrites the buffers
+    }
+    };
     const bool full = y0 + kOutH <= p.Oy && x0 + kOutW <= p.Ox;
-    if (smallN && full) epilogue(BoolTag<true>{}, BoolTag<true>{});
-    else if (smallN) epilogue(BoolTag<true>{}, BoolTag<false>{});
-    else epilogue(BoolTag<false>{}, BoolTag<false>{});
+    if constexpr (kDirect) {
+        if (smallN && full) direct_epilogue(BoolTag<true>{}, BoolTag<true>{});
+        else if (smallN) direct_epilogue(BoolTag<true>{}, BoolTag<false>{});
+        else direct_epilogue(BoolTag<false>{}, BoolTag<false>{});
+    } else {
+        if (smallN && full) epilogue(BoolTag<true>{}, BoolTag<true>{});
+        else if (smallN) epilogue(BoolTag<true>{}, BoolTag<false>{});
+        else epilogue(BoolTag<false>{}, BoolTag<false>{});
+    }
 }
 
 }  // namespace
 
 bool corr_dp4a_supported(int wT, int hT) {
     return wT >= 1 && hT >= 1 && make_geom(wT, hT).smemBytes <= kMaxSmem;
+}
+
+bool corr_dp4a_direct_supported(int wT, int hT) {
+    return wT >= 1 && hT >= 1 && kOutW + wT - 1 <= kDirMaxCols &&
+           make_geom(wT, hT, true).smemBytes <= kMaxSmem;
 }
 
 cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
@@ -540,7 +683,8 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
     p.Ox = a.W - a.wT + 1;
     p.lateWave = a.overlap_prev ? kMaxCtasPerSm * sm_count() : 0;
     p.Oy = a.H - a.hT + 1;
-    p.g = make_geom(a.wT, a.hT);
+    if (a.direct && !corr_dp4a_direct_supported(a.wT, a.hT)) return cudaErrorNotSupported;
+    p.g = make_geom(a.wT, a.hT, a.direct);
 
     CUtensorMap tmap;
     memset(&tmap, 0, sizeof(tmap));
@@ -564,8 +708,8 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
     CUtensorMap tmS, tmQ;
     memset(&tmS, 0, sizeof(tmS));
     memset(&tmQ, 0, sizeof(tmQ));
-    bool tmaEpi = (a.W % 2 == 0) && ((uintptr_t)a.S % 16 == 0) && ((uintptr_t)a.Q % 16 == 0) &&
-                  p.g.epiBW <= kMaxTmaBox;
+    bool tmaEpi = !a.direct && (a.W % 2 == 0) && ((uintptr_t)a.S % 16 == 0) &&
+                  ((uintptr_t)a.Q % 16 == 0) && p.g.epiBW <= kMaxTmaBox;
     if (tmaEpi) enc = tensor_map_encoder();
     if (tmaEpi && enc) {
         const cuuint64_t dims[2] = {(cuuint64_t)a.W, (cuuint64_t)a.H};
@@ -588,9 +732,9 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
     const dim3 block(kThreads);
     const size_t smem = (size_t)p.g.smemBytes;
     cudaError_t e;
-#define NCC_LAUNCH(T, M, E, NW, HT)                                                          \
+#define NCC_LAUNCH(T, M, E, NW, HT, D)                                                       \
     do {                                                                                     \
-        e = cudaFuncSetAttribute(corr_dp4a_kernel<T, M, E, NW, HT>,                          \
+        e = cudaFuncSetAttribute(corr_dp4a_kernel<T, M, E, NW, HT, D>,                       \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);    \
         if (e != cudaSuccess) return e;                                                      \
         if (a.overlap_prev) {                                                                \
@@ -604,21 +748,23 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
             attr[0].val.programmaticStreamSerializationAllowed = 1;                          \
             cfg.attrs = attr;                                                                \
             cfg.numAttrs = 1;                                                                \
-            e = cudaLaunchKernelEx(&cfg, corr_dp4a_kernel<T, M, E, NW, HT>, tmap, tmS, tmQ, p); \
+            e = cudaLaunchKernelEx(&cfg, corr_dp4a_kernel<T, M, E, NW, HT, D>, tmap, tmS, tmQ, p); \
             if (e != cudaSuccess) return e;                                                  \
         } else {                                                                             \
-            corr_dp4a_kernel<T, M, E, NW, HT><<<grid, block, smem, stream>>>(tmap, tmS, tmQ, p); \
+            corr_dp4a_kernel<T, M, E, NW, HT, D><<<grid, block, smem, stream>>>(tmap, tmS, tmQ, p); \
         }                                                                                    \
     } while (0)
     // the fixed narrow layout only where the rows are staged by TMA; a
     // compile-time height for the common 16-row templates on that path
     const bool narrow = a.wT <= kNarrowT;
-#define NCC_LAUNCH_E(T, M)                                                  \
-    do {                                                                    \
-        if (tmaEpi && narrow && a.hT == 16) NCC_LAUNCH(T, M, true, true, 16); \
-        else if (tmaEpi && narrow) NCC_LAUNCH(T, M, true, true, 0);         \
-        else if (tmaEpi) NCC_LAUNCH(T, M, true, false, 0);                  \
-        else NCC_LAUNCH(T, M, false, false, 0);                             \
+#define NCC_LAUNCH_E(T, M)                                                         \
+    do {                                                                           \
+        if (a.direct && a.hT == 16) NCC_LAUNCH(T, M, false, false, 16, true);      \
+        else if (a.direct) NCC_LAUNCH(T, M, false, false, 0, true);                \
+        else if (tmaEpi && narrow && a.hT == 16) NCC_LAUNCH(T, M, true, true, 16, false); \
+        else if (tmaEpi && narrow) NCC_LAUNCH(T, M, true, true, 0, false);         \
+        else if (tmaEpi) NCC_LAUNCH(T, M, true, false, 0, false);                  \
+        else NCC_LAUNCH(T, M, false, false, 0, false);                             \
     } while (0)
     if (tma && moments) NCC_LAUNCH_E(true, true);
     else if (tma) NCC_LAUNCH_E(true, false);

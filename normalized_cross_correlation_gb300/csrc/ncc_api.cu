@@ -90,6 +90,18 @@ int host_path_pool(cudaMemPool_t *out) {
     return NCC_OK;
 }
 
+// Arguments of the direct-moment calls (no tables).
+int check_direct(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT, int nT) {
+    int rc = check_image(img, W, H);
+    if (rc != NCC_OK) return rc;
+    if (!tmpl || wT < 1 || hT < 1 || nT < 1 || wT > W || hT > H) return NCC_ERR_INVALID_ARG;
+    if ((long long)wT * hT > kMaxN) return NCC_ERR_UNSUPPORTED;
+    if ((long long)nT * (W - wT + 1) * (long long)(H - hT + 1) >= (1ll << 40))
+        return NCC_ERR_UNSUPPORTED;
+    if (!ncc::corr_dp4a_direct_supported(wT, hT)) return NCC_ERR_UNSUPPORTED;
+    return NCC_OK;
+}
+
 int to_status(cudaError_t e) {
     if (e == cudaSuccess) return NCC_OK;
     if (e == cudaErrorMemoryAllocation) return NCC_ERR_NOMEM;
@@ -101,7 +113,8 @@ int to_status(cudaError_t e) {
 // of img, so a single-template launch may overlap its tail.
 int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT, int nT,
                   const int64_t *S, const int64_t *Q, float *out, int64_t *sumI,
-                  int64_t *sumI2, int64_t *sumIT, cudaStream_t stream, bool after_sat = false) {
+                  int64_t *sumI2, int64_t *sumIT, cudaStream_t stream, bool after_sat = false,
+                  bool direct = false) {
     int *status = nullptr;
     int rc = status_ptr(&status);
     if (rc != NCC_OK) return rc;
@@ -112,12 +125,13 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
         std::lock_guard<std::mutex> lock(g_mutex);
         path = g_path;
     }
-    if (nT > 1 && ncc::bank_tc_supported(W, H, wT, hT, nT)) {
+    if (!direct && nT > 1 && ncc::bank_tc_supported(W, H, wT, hT, nT)) {
         ncc::BankArgs b{img, W, H, tmpl, wT, hT, nT, S, Q, out, sumI, sumI2, sumIT, status};
         rc = to_status(ncc::bank_tc_launch(b, stream));
         if (rc == NCC_OK) g_last_path = NCC_PATH_BANK;
         return rc;
     }
+    if (direct) path = NCC_PATH_DP4A;  // the direct moments exist on the dp4a kernel only
     if (path != NCC_PATH_TENSOR && !ncc::corr_dp4a_supported(wT, hT)) return NCC_ERR_UNSUPPORTED;
     int used = NCC_PATH_NONE;
     for (int t = 0; t < nT; ++t) {
@@ -133,6 +147,7 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
         a.sumIT = sumIT ? sumIT + (size_t)t * plane : nullptr;
         a.status = status;
         a.overlap_prev = after_sat && t == 0;
+        a.direct = direct;
         cudaError_t e = cudaErrorNotSupported;
         // Automatic selection takes the dp4a kernel: on the 4096x4096 /
         // 16x16 workload it measures faster than the tensor-core kernel
@@ -241,6 +256,34 @@ int ncc_correlate_moments(const uint8_t *img, int W, int H, const uint8_t *tmpl,
         return NCC_ERR_INVALID_ARG;
     return run_correlate(img, W, H, tmpl, wT, hT, nT, S, Q, nullptr, sumI, sumI2, sumIT,
                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int ncc_correlate_direct(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT,
+                         int nT, float *out, ncc_stream_t stream) {
+    int rc = check_direct(img, W, H, tmpl, wT, hT, nT);
+    if (rc != NCC_OK) return rc;
+    if (!out || (uintptr_t)out % 4) return NCC_ERR_INVALID_ARG;
+    const size_t nout = (size_t)nT * (W - wT + 1) * (H - hT + 1) * sizeof(float);
+    if (overlaps(out, nout, img, (size_t)W * H) || overlaps(out, nout, tmpl, (size_t)nT * wT * hT))
+        return NCC_ERR_INVALID_ARG;
+    return run_correlate(img, W, H, tmpl, wT, hT, nT, nullptr, nullptr, out, nullptr, nullptr,
+                         nullptr, reinterpret_cast<cudaStream_t>(stream), false, true);
+}
+
+int ncc_correlate_direct_moments(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
+                                 int hT, int nT, int64_t *sumI, int64_t *sumI2, int64_t *sumIT,
+                                 ncc_stream_t stream) {
+    int rc = check_direct(img, W, H, tmpl, wT, hT, nT);
+    if (rc != NCC_OK) return rc;
+    if (!sumI || !sumI2 || !sumIT || (uintptr_t)sumI % 8 || (uintptr_t)sumI2 % 8 ||
+        (uintptr_t)sumIT % 8)
+        return NCC_ERR_INVALID_ARG;
+    const size_t plane = (size_t)(W - wT + 1) * (H - hT + 1) * 8;
+    if (overlaps(sumI, plane, sumI2, plane) || overlaps(sumI, plane, sumIT, plane * nT) ||
+        overlaps(sumI2, plane, sumIT, plane * nT))
+        return NCC_ERR_INVALID_ARG;
+    return run_correlate(img, W, H, tmpl, wT, hT, nT, nullptr, nullptr, nullptr, sumI, sumI2,
+                         sumIT, reinterpret_cast<cudaStream_t>(stream), false, true);
 }
 
 int ncc_match(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT, int nT,

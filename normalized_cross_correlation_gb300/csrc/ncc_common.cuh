@@ -152,10 +152,15 @@ struct CorrArgs {
     // it waits on that grid, and S and Q after.  Only for a previous kernel
     // that writes neither img nor tmpl.
     bool overlap_prev = false;
+    // Window moments from the staged image tile (sliding column sums and row
+    // prefixes in shared memory) instead of from S and Q, which are unused.
+    bool direct = false;
 };
 // Multiprocessors of the current device (cached per device).
 int sm_count();
 bool corr_dp4a_supported(int wT, int hT);
+// The same with direct window moments (CorrArgs::direct): wT <= 129.
+bool corr_dp4a_direct_supported(int wT, int hT);
 cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream);
 // The same on the tensor cores (tcgen05; hT <= 16, wT*hT <= 258, wT <= 126,
 // W a multiple of 16, 16-byte aligned img, S and Q).  Returns

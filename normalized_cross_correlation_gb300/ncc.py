@@ -27,6 +27,7 @@ NCC_SAT_NAIVE = 1      # one thread per row, then one thread per column
 NCC_SAT_TWO_PASS = 2   # uint32 row sums, then a column look-back scan
 
 EXPORTS = ("ncc_sat_build", "ncc_sat_build_noalloc", "ncc_sat_build_variant", "ncc_correlate", "ncc_correlate_bank", "ncc_correlate_moments",
+           "ncc_correlate_direct", "ncc_correlate_direct_moments",
            "ncc_match", "ncc_match_host", "ncc_sync_status", "ncc_status_string", "ncc_version",
            "ncc_debug_set_fault", "ncc_debug_set_path", "ncc_debug_last_path")
 
@@ -62,6 +63,8 @@ def lib() -> ctypes.CDLL:
             L.ncc_correlate.argtypes = [vp, i, i, vp, i, i, vp, vp, vp, vp]
             L.ncc_correlate_bank.argtypes = [vp, i, i, vp, i, i, i, vp, vp, vp, vp]
             L.ncc_correlate_moments.argtypes = [vp, i, i, vp, i, i, i, vp, vp, vp, vp, vp, vp]
+            L.ncc_correlate_direct.argtypes = [vp, i, i, vp, i, i, i, vp, vp]
+            L.ncc_correlate_direct_moments.argtypes = [vp, i, i, vp, i, i, i, vp, vp, vp, vp]
             L.ncc_match.argtypes = [vp, i, i, vp, i, i, i, vp, vp, vp, vp]
             L.ncc_match_host.argtypes = [vp, i, i, vp, i, i, i, vp, vp]
             L.ncc_sync_status.argtypes = [vp]
@@ -211,6 +214,45 @@ def ncc_correlate_moments(img, tmpls, S, Q, stream=None):
                                        S.data_ptr(), Q.data_ptr(), sI.data_ptr(),
                                        sI2.data_ptr(), sIT.data_ptr(), _stream_handle(stream)),
            "ncc_correlate_moments")
+    return sI, sI2, sIT
+
+
+def ncc_correlate_direct(img, tmpls, out=None, stream=None):
+    """fp32 [nT][Oy][Ox] coefficients with the window moments taken from the
+    staged image tile (no summed-area tables)."""
+    import torch
+    _dev(img, torch.uint8, 2, "img")
+    tmpls = _tmpl3(tmpls)
+    _dev(tmpls, torch.uint8, 3, "tmpls")
+    H, W = img.shape
+    nT, hT, wT = tmpls.shape
+    if out is None:
+        out = torch.empty((nT, max(H - hT + 1, 0), max(W - wT + 1, 0)), dtype=torch.float32,
+                          device=img.device)
+    _dev(out, torch.float32, 3, "out")
+    _check(lib().ncc_correlate_direct(img.data_ptr(), W, H, tmpls.data_ptr(), wT, hT, nT,
+                                      out.data_ptr(), _stream_handle(stream)),
+           "ncc_correlate_direct")
+    return out
+
+
+def ncc_correlate_direct_moments(img, tmpls, stream=None):
+    """(SumI [Oy][Ox], SumI2 [Oy][Ox], SumIT [nT][Oy][Ox]) as int64, the
+    moments taken from the staged image tile."""
+    import torch
+    _dev(img, torch.uint8, 2, "img")
+    tmpls = _tmpl3(tmpls)
+    _dev(tmpls, torch.uint8, 3, "tmpls")
+    H, W = img.shape
+    nT, hT, wT = tmpls.shape
+    Oy, Ox = max(H - hT + 1, 0), max(W - wT + 1, 0)
+    sI = torch.empty((Oy, Ox), dtype=torch.int64, device=img.device)
+    sI2 = torch.empty((Oy, Ox), dtype=torch.int64, device=img.device)
+    sIT = torch.empty((nT, Oy, Ox), dtype=torch.int64, device=img.device)
+    _check(lib().ncc_correlate_direct_moments(img.data_ptr(), W, H, tmpls.data_ptr(), wT, hT, nT,
+                                              sI.data_ptr(), sI2.data_ptr(), sIT.data_ptr(),
+                                              _stream_handle(stream)),
+           "ncc_correlate_direct_moments")
     return sI, sI2, sIT
 
 

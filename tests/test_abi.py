@@ -67,6 +67,15 @@ def test_argument_checks_need_no_gpu(built_lib):
     assert L.ncc_correlate(fake, 16, 16, fake * 2, 4, 4, fake * 8, fake * 16, fake * 8,
                            None) == ncc.NCC_ERR_INVALID_ARG
     assert L.ncc_match_host(None, 16, 16, fake, 4, 4, 1, fake, None) == ncc.NCC_ERR_INVALID_ARG
+    # the direct-moment calls: wider than 129 is refused, missing image, output over the image
+    assert L.ncc_correlate_direct(fake, 200, 40, fake * 16, 130, 4, 1, fake * 32,
+                                  None) == ncc.NCC_ERR_UNSUPPORTED
+    assert L.ncc_correlate_direct(None, 200, 40, fake * 16, 16, 4, 1, fake * 32,
+                                  None) == ncc.NCC_ERR_INVALID_ARG
+    assert L.ncc_correlate_direct(fake, 200, 40, fake * 16, 16, 4, 1, fake + 64,
+                                  None) == ncc.NCC_ERR_INVALID_ARG
+    assert L.ncc_correlate_direct_moments(fake, 200, 40, fake * 16, 16, 4, 1, fake * 32,
+                                          fake * 32 + 8, fake * 64, None) == ncc.NCC_ERR_INVALID_ARG
     # the combined call: missing image, overlapping tables, a table over the templates
     assert L.ncc_match(None, 16, 16, fake * 2, 4, 4, 1, fake * 8, fake * 16, fake * 32,
                        None) == ncc.NCC_ERR_INVALID_ARG
