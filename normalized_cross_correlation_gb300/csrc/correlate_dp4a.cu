@@ -279,10 +279,8 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     // SM's copies are served in order, and the tile is needed first.  The
     // CTAs of the first wave of an overlapped launch may start before the
     // tables are complete: they request them after their numerator.
-    // (recomputed where used: a flag kept live across the numerator costs a
-    // register the numerator needs)
-    auto late_issue = [&]() { return (int)(blockIdx.y * gridDim.x + blockIdx.x) < p.lateWave; };
-    if (kTmaEpi && tid == 0 && !late_issue()) {
+    const bool lateIssue = (int)(blockIdx.y * gridDim.x + blockIdx.x) < p.lateWave;
+    if (kTmaEpi && tid == 0 && !lateIssue) {
         grid_dependency_wait();
         for (int t = 0; t < kEpiStages && t < epiSteps; ++t) issue_epi(t);
     }
@@ -418,7 +416,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         }
     }
 
-    if (kTmaEpi && tid == 0 && late_issue()) {
+    if (kTmaEpi && tid == 0 && lateIssue) {
         grid_dependency_wait();
         for (int t = 0; t < kEpiStages && t < epiSteps; ++t) issue_epi(t);
     }
