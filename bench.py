@@ -70,6 +70,7 @@ NCU_TRAFFIC_BYTES = {
     ("sat_build", "ncc_4096_t16"): 230.7e6,
     ("corr_dp4a", "ncc_4096_t16"): 348.9e6,
     ("bank_tc", "bank_2048_64x16"): 1075.6e6,
+    ("corr_dp4a_direct", "ncc_4096_t16"): 26.4e6,
 }
 
 
@@ -478,10 +479,10 @@ def run_gpu_direct(args, w: inputs.Workload) -> dict | None:
     corr_bytes = 4 * coeffs + w.W * w.H * nT      # coefficients out, the image once per template
     r_alu = {"kernel": "corr_dp4a_direct", "bound": "alu", "achieved": dp4a / (ms * 1e-3) / 1e12,
              "peak": alu_peak / 1e12, "unit": "Tdp4a/s", "frac": dp4a / (ms * 1e-3) / alu_peak,
-             "traffic": None}
+             "traffic": NCU_TRAFFIC_BYTES.get(("corr_dp4a_direct", w.name))}
     gbs = corr_bytes / (ms * 1e-3) / 1e9
     r_hbm = {"kernel": "corr_dp4a_direct", "bound": "hbm", "achieved": gbs, "peak": hbm,
-             "unit": "GB/s", "frac": gbs / hbm, "traffic": None}
+             "unit": "GB/s", "frac": gbs / hbm, "traffic": r_alu["traffic"]}
     dominant = max(r_alu, r_hbm, key=lambda r: r["frac"])
     return {
         "metric": f"NCC coefficients/s ({w.name}, direct moments)", "value": value, "unit": UNIT,
