@@ -70,7 +70,7 @@ NCU_TRAFFIC_BYTES = {
     ("sat_build", "ncc_4096_t16"): 230.7e6,
     ("corr_dp4a", "ncc_4096_t16"): 348.9e6,
     ("bank_tc", "bank_2048_64x16"): 1075.6e6,
-    ("corr_dp4a_direct", "ncc_4096_t16"): 26.4e6,
+    # the direct kernel changed since its capture: no figure until re-captured
 }
 
 

@@ -210,7 +210,8 @@ __device__ __forceinline__ void mbar_wait(unsigned long long *bar, uint32_t pari
     }
 }
 
-// kNarrow: the template is at most kNarrowT wide (fixed staged layout).
+// kNarrow: the template is at most kNarrowT wide (fixed staged layout; with
+// kDirect, a fixed row-prefix pass).
 // kHT: the template height when fixed at compile time (0: run time).
 // kDirect: window moments from the staged tile, not from S and Q.
 template <bool kTma, bool kMoments, bool kTmaEpi, bool kNarrow, int kHT, bool kDirect>
@@ -579,6 +580,43 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         __syncthreads();
         // (2) exclusive prefix of every stored row, in place: entry e holds
         //     the sum of columns 0 .. e-1 (entry ncols the whole row)
+        if constexpr (kNarrow) {
+            // at most kOutW + kNarrowT - 1 columns: 5 per lane, both tables
+            // of a row in one pass
+            constexpr int kPer = (kOutW + kNarrowT - 1 + 31) / 32;
+            for (int rr = warp; rr < kDirRows; rr += kWarps) {
+                uint32_t *r1 = P1 + rr * cP, *r2 = P2 + rr * cP;
+                uint32_t a[kPer], b[kPer], ra = 0, rb = 0;
+#pragma unroll
+                for (int j = 0; j < kPer; ++j) {
+                    const int c = lane * kPer + j;
+                    const bool in = c < ncols;
+                    ra += in ? r1[c] : 0u;
+                    rb += in ? r2[c] : 0u;
+                    a[j] = ra;
+                    b[j] = rb;
+                }
+                uint32_t ia = ra, ib = rb;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t ua = __shfl_up_sync(0xffffffffu, ia, o);
+                    const uint32_t ub = __shfl_up_sync(0xffffffffu, ib, o);
+                    if (lane >= o) { ia += ua; ib += ub; }
+                }
+                ia -= ra;
+                ib -= rb;
+                __syncwarp();                         // every lane has read its columns
+#pragma unroll
+                for (int j = 0; j < kPer; ++j) {
+                    const int c = lane * kPer + j;
+                    if (c < ncols) {
+                        r1[c + 1] = ia + a[j];
+                        r2[c + 1] = ib + b[j];
+                    }
+                }
+                if (lane == 0) { r1[0] = 0u; r2[0] = 0u; }
+            }
+        } else
         for (int task = warp; task < 2 * kDirRows; task += kWarps) {
             uint32_t *rowp = (task < kDirRows ? P1 : P2) + (task % kDirRows) * cP;
             uint32_t s[8];
@@ -757,7 +795,8 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
     const bool narrow = a.wT <= kNarrowT;
 #define NCC_LAUNCH_E(T, M)                                                         \
     do {                                                                           \
-        if (a.direct && a.hT == 16) NCC_LAUNCH(T, M, false, false, 16, true);      \
+        if (a.direct && narrow && a.hT == 16) NCC_LAUNCH(T, M, false, true, 16, true); \
+        else if (a.direct && narrow) NCC_LAUNCH(T, M, false, true, 0, true);       \
         else if (a.direct) NCC_LAUNCH(T, M, false, false, 0, true);                \
         else if (tmaEpi && narrow && a.hT == 16) NCC_LAUNCH(T, M, true, true, 16, false); \
         else if (tmaEpi && narrow) NCC_LAUNCH(T, M, true, true, 0, false);         \
