@@ -78,6 +78,10 @@ enum ncc_status_code {
  * larger image needs more room -- make such a call before any stream
  * capture -- and reused afterwards without clearing.  Calls on different
  * streams are ordered through an event so they never share it concurrently.
+ * The build kernel lets a kernel launched after it with programmatic stream
+ * serialization start before it ends (ncc_match uses this); such a kernel
+ * must wait on the grid dependency before it reads S or Q.  Ordinary
+ * stream order is unaffected.
  * Returns NCC_OK, NCC_ERR_INVALID_ARG, NCC_ERR_UNSUPPORTED, NCC_ERR_NOMEM or
  * NCC_ERR_CUDA.
  */
