@@ -462,7 +462,9 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     // (every output row and column valid: no per-output bounds checks)
     auto epilogue = [&](auto smallTag, auto fullTag) {
     constexpr bool kSmall = decltype(smallTag)::value, kFull = decltype(fullTag)::value;
-    for (int t = 0; t < epiSteps; ++t) {
+    const size_t ox2 = 2 * (size_t)p.Ox, ox4 = 2 * ox2;
+    float *outRow = p.out + (size_t)(y0 + h) * p.Ox + x;   // row y0 + 4t + h, column x
+    for (int t = 0; t < epiSteps; ++t, outRow += ox4) {
         const int st = t % kEpiStages;
         const uint32_t par = (uint32_t)((t / kEpiStages) & 1);
         // this thread's output rows of the step: h and h + 2
@@ -502,20 +504,19 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         if (kFull || (y < p.Oy && x < p.Ox)) {
             const unsigned sumIT = sIT[row * kOutW + xs];
             const size_t o = (size_t)y * p.Ox + x;
+            float *const op = outRow + (q ? ox2 : (size_t)0);
             if (kMoments) {
                 p.sumI[o] = (long long)sI;
                 p.sumI2[o] = (long long)sI2;
                 p.sumIT[o] = (long long)sumIT;
             } else {
                 float num, vIf;
-                bool vIpos;
                 if (kSmall) {
                     // both terms exactly by wrapping 32-bit products, then
                     // one rounding each
                     num = (float)(int)(Nu * sumIT - sI * sTu);
                     const uint32_t vIu = Nu * sI2 - sI * sI;
-                    vIpos = vIu != 0u;
-                    vIf = (float)vIu;
+                    vIf = (float)max(vIu, 1u);
                 } else {
                     // SumI < 2^25 and SumT < 2^25; SumI2 < 2^32
                     const long long numi = (long long)((unsigned long long)N * sumIT) -
@@ -523,14 +524,13 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                     const long long vI = (long long)((unsigned long long)N * sI2) -
                                          (long long)sI * (long long)sI;
                     num = i64_to_f32(numi);
-                    vIpos = vI > 0;
-                    vIf = vIpos ? u64_to_f32((unsigned long long)vI) : 1.f;
+                    vIf = u64_to_f32((unsigned long long)max(vI, 1ll));
                 }
-                // invSqrtVT is 0 for a zero-variance template; vIf >= 1
-                // whenever vIpos, so the product is finite where it is kept
+                // A window of zero variance has num = 0 exactly (all its pixels
+                // are equal), so with vIf >= 1 its coefficient is +0 without
+                // a select; invSqrtVT is 0 for a zero-variance template.
                 const float rr = num * rsqrt_approx(vIf) * invSqrtVT;
-                const float r = vIpos ? fminf(1.0f, fmaxf(-1.0f, rr)) : 0.0f;
-                __stcs(p.out + o, r);
+                __stcs(op, fminf(1.0f, fmaxf(-1.0f, rr)));
             }
         }
         }
@@ -644,6 +644,8 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         }
         __syncthreads();
         // (3) coefficients of the pass's rows: thread = column xo, rows h, h+2, ..
+        float *const outPass = p.out + (size_t)(y0 + yb + h) * p.Ox + x;
+        const size_t ox2 = 2 * (size_t)p.Ox;
 #pragma unroll 2
         for (int i = 0; i < kDirRows / 2; ++i) {
             const int r = h + 2 * i, row = yb + r, y = y0 + row;
@@ -658,24 +660,20 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                     p.sumIT[o] = (long long)sumIT;
                 } else {
                     float num, vIf;
-                    bool vIpos;
                     if (kSmall) {
                         num = (float)(int)(Nu * sumIT - sI * sTu);
                         const uint32_t vIu = Nu * sI2 - sI * sI;
-                        vIpos = vIu != 0u;
-                        vIf = (float)vIu;
+                        vIf = (float)max(vIu, 1u);
                     } else {
                         const long long numi = (long long)((unsigned long long)N * sumIT) -
                                                (long long)sI * (long long)sT;
                         const long long vI = (long long)((unsigned long long)N * sI2) -
                                              (long long)sI * (long long)sI;
                         num = i64_to_f32(numi);
-                        vIpos = vI > 0;
-                        vIf = vIpos ? u64_to_f32((unsigned long long)vI) : 1.f;
+                        vIf = u64_to_f32((unsigned long long)max(vI, 1ll));
                     }
                     const float rr = num * rsqrt_approx(vIf) * invSqrtVT;
-                    const float rc = vIpos ? fminf(1.0f, fmaxf(-1.0f, rr)) : 0.0f;
-                    __stcs(p.out + o, rc);
+                    __stcs(outPass + (size_t)i * ox2, fminf(1.0f, fmaxf(-1.0f, rr)));
                 }
             }
         }
