@@ -143,6 +143,11 @@ struct BoolTag {
     static constexpr bool value = B;
 };
 
+template <int I>
+struct IntTag {
+    static constexpr int value = I;
+};
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -464,16 +469,14 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     constexpr bool kSmall = decltype(smallTag)::value, kFull = decltype(fullTag)::value;
     const size_t ox2 = 2 * (size_t)p.Ox, ox4 = 2 * ox2;
     float *outRow = p.out + (size_t)(y0 + h) * p.Ox + x;   // row y0 + 4t + h, column x
-    for (int t = 0; t < epiSteps; ++t, outRow += ox4) {
-        const int st = t % kEpiStages;
+    auto step = [&](int t, auto stTag) {
+        constexpr int st = decltype(stTag)::value;
         const uint32_t par = (uint32_t)((t / kEpiStages) & 1);
         // this thread's output rows of the step: h and h + 2
         uint32_t sIv[2] = {0, 0}, sI2v[2] = {0, 0};
         if (kTmaEpi) {
-            // one lane polls the stage's barrier for the warp
-            uint32_t done = 0;
-            if (lane == 0) done = mbar_try(&s_ebar[st], par);
-            if (!__shfl_sync(0xffffffffu, done, 0)) mbar_wait(&s_ebar[st], par, p.status);
+            // the whole warp polls the stage's barrier (a uniform wait)
+            if (!mbar_try(&s_ebar[st], par)) mbar_wait(&s_ebar[st], par, p.status);
             const uint32_t *b = reinterpret_cast<const uint32_t *>(epi + st * kEpiBufs * epiBuf);
             const int box = epiBuf / 4;                            // u32 words per box
 #pragma unroll
@@ -538,6 +541,14 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
             mbar_wait(&s_efree[st], par, p.status);              // all warps released the stage
             issue_epi(t + kEpiStages);
         }
+        outRow += ox4;
+    };
+    // steps in pairs, so that each step's ring stage (and with it every
+    // staged-row address) is a compile-time constant
+    static_assert(kEpiStages == 2, "steps go in pairs, one per ring stage");
+    for (int t = 0; t < epiSteps; t += 2) {
+        step(t, IntTag<0>{});
+        if (t + 1 < epiSteps) step(t + 1, IntTag<1>{});
     }
     };
     // Direct moments.  Per pass of kDirRows output rows: (1) thread t keeps
