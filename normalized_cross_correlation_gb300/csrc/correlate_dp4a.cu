@@ -488,6 +488,12 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_efree[st]);           // this warp is done with the stage
+            // the refill of this stage for step t+2 goes out as soon as every
+            // warp has read it, before this step's arithmetic
+            if (tid == 0 && t + kEpiStages < epiSteps) {
+                mbar_wait(&s_efree[st], par, p.status);          // all warps released the stage
+                issue_epi(t + kEpiStages);
+            }
         }
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -536,10 +542,6 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                 __stcs(op, fminf(1.0f, fmaxf(-1.0f, rr)));
             }
         }
-        }
-        if (kTmaEpi && tid == 0 && t + kEpiStages < epiSteps) {
-            mbar_wait(&s_efree[st], par, p.status);              // all warps released the stage
-            issue_epi(t + kEpiStages);
         }
         outRow += ox4;
     };
