@@ -27,16 +27,28 @@
 //   - The template is packed into 32-bit words in shared memory, in chunks of
 //     16 pixels, zero-padded to a multiple of 16 (the zero bytes cancel any
 //     pixels read past the window).
-//   - SumIT accumulates in uint32 (exact while wT*hT*255^2 < 2^32).
+//   - SumIT accumulates in uint32 (exact while wT*hT*255^2 < 2^32).  16-row
+//     templates get an instantiation with the height fixed at compile time.
 //   - Epilogue: the SumIT tile is transposed through shared memory (over the
-//     dead image tile); the CTA then walks its output rows four at a time,
-//     one shift and two rows per thread.  The table rows a step needs (S and
-//     Q at rows y-1.. and y+hT-1.., columns x0-2 .. x0+wT+127) arrive as four
-//     TMA boxes of four rows each into a two-stage ring -- few, large
+//     dead image tile, columns swizzled so that neither the stores nor the
+//     row reads conflict); the CTA then walks its output rows four at a
+//     time, one shift and two rows per thread.  The table rows a step needs
+//     (S and Q at rows y-1.. and y+hT-1.., columns x0-2 .. x0+wT+127) arrive
+//     as four TMA boxes of four rows each into a two-stage ring -- few, large
 //     requests, since each TMA request costs about a hundred cycles to
-//     issue.  The first stages are issued before the numerator loop.  TMA's
-//     zero fill outside the tables implements the four-corner rule's row -1
-//     / column -1 = 0.  (Tables whose rows are not a multiple of 16 bytes, or
+//     issue.  The first two stages are requested right after the image tile
+//     (one SM's requests are served in order); a stage is refilled as soon
+//     as every warp has read it.  Steps go in pairs, one per ring stage, so
+//     the staged-row addresses are compile-time offsets.  TMA's zero fill
+//     outside the tables implements the four-corner rule's row -1 / column
+//     -1 = 0.
+//   - Launched after the SAT build with programmatic stream serialization
+//     (ncc_match), the kernel may start before the tables are complete: it
+//     waits on the grid dependency before the first table-row request (the
+//     first wave of CTAs makes that request after its numerator).
+//   - Direct moments (kDirect): SumI and SumI2 come from the staged tile
+//     instead of S and Q, by sliding column sums and row prefixes in shared
+//     memory, 16 output rows per pass.  (Tables whose rows are not a multiple of 16 bytes, or
 //     templates wider than 127, read the corners with global loads.)  The
 //     four-corner sums use the low 32 bits of the table entries (exact: the
 //     sums are below 2^32); templates of at most 363 pixels form the
