@@ -67,6 +67,7 @@ constexpr int kOutW = 128;
 constexpr int kRowsPerThread = 8;
 constexpr int kWarps = 8;
 constexpr int kOutH = kWarps * kRowsPerThread;  // 64
+constexpr int kSmallRPT = 4;   // rows per thread of the small-map kernels (tiles of 128 x 32)
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxCtasPerSm = 3;   // resident CTAs per SM (launch bound)
 constexpr int kMaxTmaBox = 256;        // TMA box extent limit per dimension
@@ -95,7 +96,7 @@ constexpr int kDirMaxCols = kThreads;
 struct Geom {
     int nch;         // 16-pixel template chunks
     int boxW;        // staged tile width in bytes = kOutW + 16*nch
-    int boxH;        // staged tile height = kOutH + hT - 1
+    int boxH;        // staged tile height = output rows + hT - 1
     int tmplOff;     // offset of the packed template (after the tile / SumIT region)
     int epiBW;       // table-row segment length (int64 elements), even
     int epiBuf;      // bytes per box (kEpiRowsPerStep table-row segments, 128-aligned)
@@ -109,13 +110,13 @@ struct Geom {
 // direct: the window moments come from the staged tile (the tile outlives
 // the numerator, so the SumIT transpose gets its own space) instead of from
 // the summed-area tables.
-Geom make_geom(int wT, int hT, bool direct = false) {
+Geom make_geom(int wT, int hT, bool direct = false, int tileH = kOutH) {
     Geom g;
     g.nch = (wT + 15) / 16;
     g.boxW = kOutW + 16 * g.nch;
-    g.boxH = kOutH + hT - 1;
+    g.boxH = tileH + hT - 1;
     const int tileBytes = (g.boxW * g.boxH + 127) / 128 * 128;
-    const int sumBytes = kOutH * kOutW * 4;  // the SumIT transpose reuses the tile's space
+    const int sumBytes = tileH * kOutW * 4;  // the SumIT transpose reuses the tile's space
     if (direct) {
         g.tmplOff = tileBytes;
         g.sumOff = (g.tmplOff + hT * g.nch * 16 + 127) / 128 * 128;
@@ -231,10 +232,12 @@ __device__ __forceinline__ void mbar_wait(unsigned long long *bar, uint32_t pari
 // kDirect, a fixed row-prefix pass).
 // kHT: the template height when fixed at compile time (0: run time).
 // kDirect: window moments from the staged tile, not from S and Q.
-template <bool kTma, bool kMoments, bool kTmaEpi, bool kNarrow, int kHT, bool kDirect>
+// kRPT: output rows per thread (8; 4 for maps too small to fill the GPU).
+template <bool kTma, bool kMoments, bool kTmaEpi, bool kNarrow, int kHT, bool kDirect, int kRPT>
 __global__ void __launch_bounds__(kThreads, kMaxCtasPerSm)
 corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmS,
                  const __grid_constant__ CUtensorMap tmQ, const KParams p) {
+    constexpr int kTileH = kWarps * kRPT;  // output rows per tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -248,8 +251,8 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     const Geom &g = p.g;
     const int epiBW = kNarrow ? kNarrowBW : g.epiBW, epiBuf = kNarrow ? kNarrowBuf : g.epiBuf;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int x0 = blockIdx.x * kOutW, y0 = blockIdx.y * kOutH;
-    const int epiSteps = (min(kOutH, p.Oy - y0) + kEpiRowsPerStep - 1) / kEpiRowsPerStep;
+    const int x0 = blockIdx.x * kOutW, y0 = blockIdx.y * kTileH;
+    const int epiSteps = (min(kTileH, p.Oy - y0) + kEpiRowsPerStep - 1) / kEpiRowsPerStep;
     uint8_t *epi = smem + g.epiOff;
     // table-row segments of epilogue step t: rows y0+2t+h, buffers
     // [stage][h][S top, S bottom, Q top, Q bottom]
@@ -357,14 +360,14 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     const int qg = lane >> 2, d = lane & 3;
     const uint32_t sel = 0x3210u + 0x1111u * (uint32_t)d;
     const uint8_t *cp = smem + 16 * qg;
-    uint32_t acc[kRowsPerThread][4];
+    uint32_t acc[kRPT][4];
 #pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i)
+    for (int i = 0; i < kRPT; ++i)
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[i][k] = 0u;
 
     for (int c = 0; c < g.nch; ++c) {
-        const uint8_t *cc = cp + 16 * c + warp * kRowsPerThread * g.boxW;
+        const uint8_t *cc = cp + 16 * c + warp * kRPT * g.boxW;
         const uint4 *tc = reinterpret_cast<const uint4 *>(tw) + c * hT;  // chunk c of row j at tc[j]
         // the d-shifted words of tile row r of this warp
         auto row_words = [&](int r, uint32_t (&v)[7]) {
@@ -388,11 +391,11 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                 a[k] = s;
             }
         };
-        if (hT >= kRowsPerThread) {
+        if (hT >= kRPT) {
             // tile row r meets output rows i = max(0, r-hT+1) .. min(7, r):
             // ramp-up rows, full rows and ramp-down rows, without branches
 #pragma unroll
-            for (int r = 0; r < kRowsPerThread - 1; ++r) {
+            for (int r = 0; r < kRPT - 1; ++r) {
                 uint32_t v[7];
                 row_words(r, v);
 #pragma unroll
@@ -402,31 +405,31 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                 uint32_t v[7];
                 row_words(r, v);
 #pragma unroll
-                for (int i = 0; i < kRowsPerThread; ++i) mac(acc[i], v, tc[r - i]);
+                for (int i = 0; i < kRPT; ++i) mac(acc[i], v, tc[r - i]);
             };
             if constexpr (kHT != 0) {
                 // fixed height: the phase unrolls and the template rows it
                 // reads stay in registers from one tile row to the next
 #pragma unroll
-                for (int r = kRowsPerThread - 1; r < kHT; ++r) full_row(r);
+                for (int r = kRPT - 1; r < kHT; ++r) full_row(r);
             } else {
-                for (int r = kRowsPerThread - 1; r < hT; ++r) full_row(r);
+                for (int r = kRPT - 1; r < hT; ++r) full_row(r);
             }
 #pragma unroll
-            for (int m = 0; m < kRowsPerThread - 1; ++m) {
+            for (int m = 0; m < kRPT - 1; ++m) {
                 const int r = hT + m;
                 uint32_t v[7];
                 row_words(r, v);
 #pragma unroll
-                for (int i = m + 1; i < kRowsPerThread; ++i) mac(acc[i], v, tc[r - i]);
+                for (int i = m + 1; i < kRPT; ++i) mac(acc[i], v, tc[r - i]);
             }
         } else {
-            const int rows = kRowsPerThread + hT - 1;
+            const int rows = kRPT + hT - 1;
             for (int r = 0; r < rows; ++r) {
                 uint32_t v[7];
                 row_words(r, v);
 #pragma unroll
-                for (int i = 0; i < kRowsPerThread; ++i) {
+                for (int i = 0; i < kRPT; ++i) {
                     const int j = r - i;
                     if (j >= 0 && j < hT) mac(acc[i], v, tc[j]);
                 }
@@ -441,7 +444,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
 
     // --- transpose SumIT through shared memory ------------------------------
     __syncthreads();  // every warp is done with the staged copies
-    // [kOutH][kOutW], column c stored at c ^ (((c >> 5) & 3) << 2): the
+    // [kTileH][kOutW], column c stored at c ^ (((c >> 5) & 3) << 2): the
     // 32 lanes of one store (columns 16*qg + 4*k + d) then fall in 32
     // different banks, and a row read of 32 consecutive columns still does.
     uint32_t *sIT = reinterpret_cast<uint32_t *>(smem + (kDirect ? g.sumOff : 0));
@@ -451,8 +454,8 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         for (int k = 0; k < 4; ++k) {
             const int ck = 4 * (k ^ (qg >> 1));
 #pragma unroll
-            for (int i = 0; i < kRowsPerThread; ++i)
-                sw[(warp * kRowsPerThread + i) * kOutW + ck] = acc[i][k];
+            for (int i = 0; i < kRPT; ++i)
+                sw[(warp * kRPT + i) * kOutW + ck] = acc[i][k];
         }
     }
     __syncthreads();
@@ -585,7 +588,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
             c1 += v;
             c2 += v * v;
         }
-    const int rowsValid = min(kOutH, p.Oy - y0);
+    const int rowsValid = min(kTileH, p.Oy - y0);
     const int per = (ncols + 31) >> 5;            // columns per lane in the prefix pass (<= 8)
     for (int yb = 0; yb < rowsValid; yb += kDirRows) {
         // (1) column sums of the pass's rows
@@ -595,7 +598,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
                 const int yr = yb + r;
                 P1[r * cP + tid] = c1;
                 P2[r * cP + tid] = c2;
-                if (yr + 1 < kOutH) {                 // the tile holds rows 0 .. kOutH + hT - 2
+                if (yr + 1 < kTileH) {                 // the tile holds rows 0 .. kTileH + hT - 2
                     const uint32_t a = col[(yr + p.hT) * g.boxW], b = col[yr * g.boxW];
                     c1 += a - b;
                     c2 += a * a - b * b;
@@ -705,7 +708,7 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         __syncthreads();                              // before the next pass overwrites the buffers
     }
     };
-    const bool full = y0 + kOutH <= p.Oy && x0 + kOutW <= p.Ox;
+    const bool full = y0 + kTileH <= p.Oy && x0 + kOutW <= p.Ox;
     if constexpr (kDirect) {
         if (smallN && full) direct_epilogue(BoolTag<true>{}, BoolTag<true>{});
         else if (smallN) direct_epilogue(BoolTag<true>{}, BoolTag<false>{});
@@ -743,7 +746,15 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
     p.lateWave = a.overlap_prev ? kMaxCtasPerSm * sm_count() : 0;
     p.Oy = a.H - a.hT + 1;
     if (a.direct && !corr_dp4a_direct_supported(a.wT, a.hT)) return cudaErrorNotSupported;
-    p.g = make_geom(a.wT, a.hT, a.direct);
+    // Maps too small to give every SM two tiles of 128 x 64 take tiles of
+    // 128 x 32 (four output rows per thread) on the all-TMA path.
+    const long long tiles64 =
+        (long long)((p.Ox + kOutW - 1) / kOutW) * ((p.Oy + kOutH - 1) / kOutH);
+    bool small = !a.direct && tiles64 < 2ll * sm_count() && a.wT <= 126 && a.hT <= 225 &&
+                 a.W % 16 == 0 && (uintptr_t)a.img % 16 == 0 && (uintptr_t)a.S % 16 == 0 &&
+                 (uintptr_t)a.Q % 16 == 0;
+    const int tileH = small ? kWarps * kSmallRPT : kOutH;
+    p.g = make_geom(a.wT, a.hT, a.direct, tileH);
 
     CUtensorMap tmap;
     memset(&tmap, 0, sizeof(tmap));
@@ -787,13 +798,14 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
     } else {
         tmaEpi = false;
     }
-    const dim3 grid((p.Ox + kOutW - 1) / kOutW, (p.Oy + kOutH - 1) / kOutH);
+    if (small && !(tma && tmaEpi)) return cudaErrorNotSupported;  // the checks above exclude it
+    const dim3 grid((p.Ox + kOutW - 1) / kOutW, (p.Oy + tileH - 1) / tileH);
     const dim3 block(kThreads);
     const size_t smem = (size_t)p.g.smemBytes;
     cudaError_t e;
-#define NCC_LAUNCH(T, M, E, NW, HT, D)                                                       \
+#define NCC_LAUNCH(T, M, E, NW, HT, D, R)                                                    \
     do {                                                                                     \
-        e = cudaFuncSetAttribute(corr_dp4a_kernel<T, M, E, NW, HT, D>,                       \
+        e = cudaFuncSetAttribute(corr_dp4a_kernel<T, M, E, NW, HT, D, R>,                    \
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);    \
         if (e != cudaSuccess) return e;                                                      \
         if (a.overlap_prev) {                                                                \
@@ -807,10 +819,10 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
             attr[0].val.programmaticStreamSerializationAllowed = 1;                          \
             cfg.attrs = attr;                                                                \
             cfg.numAttrs = 1;                                                                \
-            e = cudaLaunchKernelEx(&cfg, corr_dp4a_kernel<T, M, E, NW, HT, D>, tmap, tmS, tmQ, p); \
+            e = cudaLaunchKernelEx(&cfg, corr_dp4a_kernel<T, M, E, NW, HT, D, R>, tmap, tmS, tmQ, p); \
             if (e != cudaSuccess) return e;                                                  \
         } else {                                                                             \
-            corr_dp4a_kernel<T, M, E, NW, HT, D><<<grid, block, smem, stream>>>(tmap, tmS, tmQ, p); \
+            corr_dp4a_kernel<T, M, E, NW, HT, D, R><<<grid, block, smem, stream>>>(tmap, tmS, tmQ, p); \
         }                                                                                    \
     } while (0)
     // the fixed narrow layout only where the rows are staged by TMA; a
@@ -818,18 +830,28 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
     const bool narrow = a.wT <= kNarrowT;
 #define NCC_LAUNCH_E(T, M)                                                         \
     do {                                                                           \
-        if (a.direct && narrow && a.hT == 16) NCC_LAUNCH(T, M, false, true, 16, true); \
-        else if (a.direct && narrow) NCC_LAUNCH(T, M, false, true, 0, true);       \
-        else if (a.direct) NCC_LAUNCH(T, M, false, false, 0, true);                \
-        else if (tmaEpi && narrow && a.hT == 16) NCC_LAUNCH(T, M, true, true, 16, false); \
-        else if (tmaEpi && narrow) NCC_LAUNCH(T, M, true, true, 0, false);         \
-        else if (tmaEpi) NCC_LAUNCH(T, M, true, false, 0, false);                  \
-        else NCC_LAUNCH(T, M, false, false, 0, false);                             \
+        if (a.direct && narrow && a.hT == 16) NCC_LAUNCH(T, M, false, true, 16, true, 8); \
+        else if (a.direct && narrow) NCC_LAUNCH(T, M, false, true, 0, true, 8);    \
+        else if (a.direct) NCC_LAUNCH(T, M, false, false, 0, true, 8);             \
+        else if (tmaEpi && narrow && a.hT == 16) NCC_LAUNCH(T, M, true, true, 16, false, 8); \
+        else if (tmaEpi && narrow) NCC_LAUNCH(T, M, true, true, 0, false, 8);      \
+        else if (tmaEpi) NCC_LAUNCH(T, M, true, false, 0, false, 8);               \
+        else NCC_LAUNCH(T, M, false, false, 0, false, 8);                          \
     } while (0)
-    if (tma && moments) NCC_LAUNCH_E(true, true);
+    // small maps: the all-TMA kernels with four rows per thread
+#define NCC_LAUNCH_S(M)                                                                    \
+    do {                                                                                   \
+        if (narrow && a.hT == 16) NCC_LAUNCH(true, M, true, true, 16, false, kSmallRPT);   \
+        else if (narrow) NCC_LAUNCH(true, M, true, true, 0, false, kSmallRPT);             \
+        else NCC_LAUNCH(true, M, true, false, 0, false, kSmallRPT);                        \
+    } while (0)
+    if (small && moments) NCC_LAUNCH_S(true);
+    else if (small) NCC_LAUNCH_S(false);
+    else if (tma && moments) NCC_LAUNCH_E(true, true);
     else if (tma) NCC_LAUNCH_E(true, false);
     else if (moments) NCC_LAUNCH_E(false, true);
     else NCC_LAUNCH_E(false, false);
+#undef NCC_LAUNCH_S
 #undef NCC_LAUNCH_E
 #undef NCC_LAUNCH
     return cudaGetLastError();
