@@ -120,3 +120,32 @@ def test_host_entry_point_matches_device_path(ncc, W, H, wT, hT, nT, pinned):
         out.fill_(7.0)
         ncc.ncc_match_host(img, T, out)
         np.testing.assert_array_equal(out.numpy(), r0)
+
+
+def test_match_on_two_streams_at_once(ncc):
+    """Two images matched on two streams with their calls interleaved: the
+    builds share the library's look-back workspace (ordered through an
+    event) and each correlation overlaps its own stream's build."""
+    import torch
+    wa = inputs.random_case(501, 1536, 1100, 16, 16, nT=1, n_crops=1)
+    wb = inputs.random_case(502, 1024, 1400, 12, 9, nT=1, n_crops=1)
+    ref = []
+    for w in (wa, wb):
+        _, _, r0 = separate(ncc, to_dev(w.image), to_dev(w.templates))
+        ref.append(r0)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    da, ta = to_dev(wa.image), to_dev(wa.templates)
+    db, tb = to_dev(wb.image), to_dev(wb.templates)
+    torch.cuda.synchronize()
+    outs = []
+    for _ in range(3):
+        with torch.cuda.stream(sa):
+            ra = ncc.ncc_match(da, ta, stream=sa)[2]
+        with torch.cuda.stream(sb):
+            rb = ncc.ncc_match(db, tb, stream=sb)[2]
+        outs.append((ra, rb))
+    torch.cuda.synchronize()
+    assert ncc.ncc_sync_status() == 0
+    for ra, rb in outs:
+        np.testing.assert_array_equal(ra.cpu().numpy(), ref[0])
+        np.testing.assert_array_equal(rb.cpu().numpy(), ref[1])
