@@ -67,7 +67,8 @@ constexpr int kOutW = 128;
 constexpr int kRowsPerThread = 8;
 constexpr int kWarps = 8;
 constexpr int kOutH = kWarps * kRowsPerThread;  // 64
-constexpr int kSmallRPT = 4;   // rows per thread of the small-map kernels (tiles of 128 x 32)
+constexpr int kSmallRPT = 4;   // rows per thread of the 128 x 32 tiles
+constexpr int kQuadMaxHT = 64; // narrow templates up to this height run four CTAs per SM
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxCtasPerSm = 3;   // resident CTAs per SM (launch bound)
 constexpr int kMaxTmaBox = 256;        // TMA box extent limit per dimension
@@ -234,7 +235,7 @@ __device__ __forceinline__ void mbar_wait(unsigned long long *bar, uint32_t pari
 // kDirect: window moments from the staged tile, not from S and Q.
 // kRPT: output rows per thread (8; 4 for maps too small to fill the GPU).
 template <bool kTma, bool kMoments, bool kTmaEpi, bool kNarrow, int kHT, bool kDirect, int kRPT>
-__global__ void __launch_bounds__(kThreads, kMaxCtasPerSm)
+__global__ void __launch_bounds__(kThreads, (kRPT == kSmallRPT && kNarrow) ? 4 : kMaxCtasPerSm)
 corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmS,
                  const __grid_constant__ CUtensorMap tmQ, const KParams p) {
     constexpr int kTileH = kWarps * kRPT;  // output rows per tile
@@ -743,17 +744,21 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
     p.sumIT = reinterpret_cast<long long *>(a.sumIT);
     p.status = a.status;
     p.Ox = a.W - a.wT + 1;
-    p.lateWave = a.overlap_prev ? kMaxCtasPerSm * sm_count() : 0;
     p.Oy = a.H - a.hT + 1;
     if (a.direct && !corr_dp4a_direct_supported(a.wT, a.hT)) return cudaErrorNotSupported;
-    // Maps too small to give every SM two tiles of 128 x 64 take tiles of
-    // 128 x 32 (four output rows per thread) on the all-TMA path.
+    // Tiles of 128 x 32 (four output rows per thread) on the all-TMA path:
+    //   - for templates up to 16 wide and kQuadMaxHT high, whose kernel fits
+    //     four CTAs on an SM (64 registers, under 56 KB of shared memory);
+    //   - for maps too small to give every SM two tiles of 128 x 64.
     const long long tiles64 =
         (long long)((p.Ox + kOutW - 1) / kOutW) * ((p.Oy + kOutH - 1) / kOutH);
-    bool small = !a.direct && tiles64 < 2ll * sm_count() && a.wT <= 126 && a.hT <= 225 &&
-                 a.W % 16 == 0 && (uintptr_t)a.img % 16 == 0 && (uintptr_t)a.S % 16 == 0 &&
-                 (uintptr_t)a.Q % 16 == 0;
+    const bool allTma = !a.direct && a.W % 16 == 0 && (uintptr_t)a.img % 16 == 0 &&
+                        (uintptr_t)a.S % 16 == 0 && (uintptr_t)a.Q % 16 == 0;
+    const bool quad = allTma && a.wT <= kNarrowT && a.hT <= kQuadMaxHT;
+    const bool small = quad || (allTma && tiles64 < 2ll * sm_count() && a.wT <= 126 && a.hT <= 225);
     const int tileH = small ? kWarps * kSmallRPT : kOutH;
+    // the CTAs resident at once: four per SM for the narrow 128 x 32 kernels
+    p.lateWave = a.overlap_prev ? (quad ? 4 : kMaxCtasPerSm) * sm_count() : 0;
     p.g = make_geom(a.wT, a.hT, a.direct, tileH);
 
     CUtensorMap tmap;
@@ -838,7 +843,7 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
         else if (tmaEpi) NCC_LAUNCH(T, M, true, false, 0, false, 8);               \
         else NCC_LAUNCH(T, M, false, false, 0, false, 8);                          \
     } while (0)
-    // small maps: the all-TMA kernels with four rows per thread
+    // 128 x 32 tiles: the all-TMA kernels with four rows per thread
 #define NCC_LAUNCH_S(M)                                                                    \
     do {                                                                                   \
         if (narrow && a.hT == 16) NCC_LAUNCH(true, M, true, true, 16, false, kSmallRPT);   \
