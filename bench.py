@@ -68,7 +68,7 @@ N_SMS = 152
 # kernel changes, so a stale count is never reported.
 NCU_TRAFFIC_BYTES = {
     ("sat_build", "ncc_4096_t16"): 230.7e6,
-    # the correlation kernel changed since its capture: no figure until re-captured
+    ("corr_dp4a", "ncc_4096_t16"): 337.7e6,
     ("bank_tc", "bank_2048_64x16"): 1075.6e6,
     ("corr_dp4a_direct", "ncc_4096_t16"): 26.3e6,
 }
