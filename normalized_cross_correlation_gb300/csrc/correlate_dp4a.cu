@@ -9,9 +9,12 @@
 // (SumI and SumI2 of every window from S and Q by the four-corner box sum).
 //
 // GB300 design:
-//   - Output tile: 128 shifts wide by 64 rows; 256 threads; each thread owns
-//     8 rows x 4 shifts.  Lane = 4*qg + d owns the shifts x0 + 16*qg + 4*k + d
-//     (k = 0..3) of rows 8*warp .. 8*warp+7.
+//   - Output tile: 128 shifts wide by 8*kRPT rows; 256 threads; each thread
+//     owns kRPT rows x 4 shifts.  Lane = 4*qg + d owns the shifts
+//     x0 + 16*qg + 4*k + d (k = 0..3) of rows kRPT*warp .. kRPT*warp+kRPT-1.
+//     kRPT = 8 (tiles of 128 x 64, three CTAs per SM) in general; kRPT = 4
+//     (128 x 32) for templates up to 16 wide, whose kernel then fits four
+//     CTAs per SM, and for maps too small to give every SM two larger tiles.
 //   - The tile plus its (wT-1) x (hT-1) halo is one TMA box (cp.async.bulk.
 //     tensor, completion on an mbarrier).  Images whose rows are not a
 //     multiple of 16 bytes, or boxes beyond the TMA limits, use plain loads.
