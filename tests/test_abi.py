@@ -106,3 +106,26 @@ def test_product_path_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, f), errors="ignore").read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "ncc_oracle" not in text, f
+
+
+def test_binding_refuses_cpu_tensors():
+    """The device entry points take CUDA tensors only: CPU tensors raise
+    before any call, so nothing is ever computed on the host."""
+    import torch
+    from normalized_cross_correlation_gb300 import ncc
+    img = torch.zeros((64, 64), dtype=torch.uint8)
+    T = torch.zeros((8, 8), dtype=torch.uint8)
+    S = torch.zeros((64, 64), dtype=torch.int64)
+    calls = [
+        lambda: ncc.ncc_sat_build(img),
+        lambda: ncc.ncc_sat_build_variant(img, ncc.NCC_SAT_NAIVE),
+        lambda: ncc.ncc_correlate(img, T, S, S),
+        lambda: ncc.ncc_correlate_bank(img, T[None], S, S),
+        lambda: ncc.ncc_correlate_moments(img, T, S, S),
+        lambda: ncc.ncc_correlate_direct(img, T),
+        lambda: ncc.ncc_correlate_direct_moments(img, T),
+        lambda: ncc.ncc_match(img, T),
+    ]
+    for call in calls:
+        with pytest.raises(TypeError):
+            call()
