@@ -37,6 +37,9 @@ def separate(ncc, dimg, dt):
 SHAPES = [
     (1024, 768, 16, 16, 1), (523, 300, 7, 5, 1), (2048, 1100, 8, 8, 1), (1000, 260, 13, 31, 1),
     (640, 480, 16, 16, 4), (272, 200, 16, 16, 1),
+    # several templates where the bank kernel does not apply (odd width): one
+    # single-template launch per template, the first one overlapped
+    (523, 300, 7, 5, 3),
 ]
 
 
