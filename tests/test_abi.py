@@ -129,3 +129,28 @@ def test_binding_refuses_cpu_tensors():
     for call in calls:
         with pytest.raises(TypeError):
             call()
+
+
+def test_header_is_plain_c_and_links(built_lib, tmp_path):
+    """include/ncc.h compiles as strict C99 (no C++ or CUDA headers needed),
+    and a C program links against the library and calls it without a GPU."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "use_ncc.c"
+    src.write_text(
+        '#include "ncc.h"\n'
+        "int main(void) {\n"
+        "    if (ncc_version() <= 0) return 1;\n"
+        "    if (ncc_sat_build(0, 16, 16, 0, 0, 0) != NCC_ERR_INVALID_ARG) return 2;\n"
+        "    return ncc_status_string(NCC_OK)[0] == 'o' ? 0 : 3;\n"
+        "}\n")
+    exe = tmp_path / "use_ncc"
+    libdir = os.path.dirname(built_lib)
+    name = os.path.basename(built_lib)[3:-3]          # libX.so -> X
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), str(src), "-L", libdir, "-l" + name,
+                    "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    assert subprocess.run([str(exe)]).returncode == 0
