@@ -1,7 +1,7 @@
 """CPU oracle for normalized cross-correlation -- TEST INFRASTRUCTURE ONLY.
 
-Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
-``bench.py`` may import this package.  The product (the CUDA library and its
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline and
+reference legs of ``bench.py`` may import this package.  The product (the CUDA library and its
 Python binding) never touches it, and it never touches the product.
 
 The arithmetic lives in ``ncc_oracle.c`` (plain C, int64 sums, double

@@ -3,7 +3,7 @@
  * cross-correlation (NCC) template matching of 8-bit images.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
- * benchmark's CPU-baseline leg may load this code.  It shares nothing with
+ * benchmark's CPU-baseline and reference legs may load this code.  It shares nothing with
  * the CUDA library (no headers, helpers, tables or constants) and never
  * calls into it.
  *
