@@ -114,10 +114,10 @@ int ncc_sat_build_variant(const uint8_t *img, int W, int H, int64_t *S, int64_t 
 /*
  * ncc_sat_build_noalloc -- ncc_sat_build for callers that cannot allocate
  * device memory (the pages have no counterpart: it is an interface
- * addition).  Callers inside a CUDA stream capture, a host callback, a
- * real-time loop, or a framework that owns every device allocation through
- * its own pool cannot let a library call cudaMalloc/cudaFree (not
- * capturable; may synchronize the device; bypasses their budget).  This
+ * addition).  Callers inside a host callback or a real-time loop cannot let
+ * a library call cudaMalloc/cudaFree, which may synchronize the whole
+ * device; a framework that owns every device allocation through its own
+ * pool cannot let a library allocate behind its budget.  This
  * entry point allocates nothing: its look-back scratch is a fixed 8 MiB
  * array compiled into the library, which every GPU that loads the library
  * holds until the process exits.
@@ -256,40 +256,8 @@ const char *ncc_status_string(int status);
 /* Library version, (major << 16) | minor. */
 int ncc_version(void);
 
-/*
- * ncc_debug_set_fault -- test hook for the bounded waits.  While
- * suppress_tile >= 0, the SAT builder's tile with that row-major index never
- * publishes its look-back results, so every tile that depends on it waits
- * until its limit (timeout_ns; 0 restores the default of one second) runs
- * out and records NCC_ERR_TIMEOUT.  suppress_tile = -1 restores normal
- * operation.  Process-wide; not for concurrent use.
- */
-int ncc_debug_set_fault(int suppress_tile, uint64_t timeout_ns);
-
-/* Kernels a correlate call can launch (ncc_debug_last_path). */
-enum ncc_path_code {
-    NCC_PATH_NONE = 0,
-    NCC_PATH_DP4A = 1,     /* single template, integer dot products         */
-    NCC_PATH_TENSOR = 2,   /* single template, tcgen05 tensor cores          */
-    NCC_PATH_BANK = 3      /* template bank, tcgen05 tensor cores            */
-};
-
-/*
- * ncc_debug_set_path -- selects the single-template kernel that
- * ncc_correlate, ncc_correlate_moments and ncc_correlate_bank (for banks the
- * bank kernel does not take) use.  0 = automatic (dp4a), NCC_PATH_DP4A =
- * dp4a, NCC_PATH_TENSOR = tensor cores (NCC_ERR_UNSUPPORTED where they do not
- * apply).  Process-wide; not for concurrent use.
- * Returns NCC_OK, or NCC_ERR_INVALID_ARG for another value.
- */
-int ncc_debug_set_path(int path);
-
-/*
- * ncc_debug_last_path -- the kernel (ncc_path_code) launched by the most
- * recent successful correlate call of this process; NCC_PATH_NONE before
- * the first.
- */
-int ncc_debug_last_path(void);
+/* Test hooks (fault and allocation-failure injection, kernel selection)
+ * are declared in ncc_debug.h; they are not part of the computing path. */
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,69 @@
+/*
+ * ncc_debug.h -- test hooks of the GB300 normalized cross-correlation
+ * library (libncc_gb300.so).  None of them computes anything: they inject
+ * failures on the host (a look-back tile that never publishes, an
+ * allocation that fails), select between the single-template kernels, and
+ * report which kernel ran, so the tests can reach paths that a correct run
+ * on a healthy GPU never takes.  The computing path is declared in ncc.h.
+ * These are process-wide switches, not for concurrent use with other calls.
+ */
+#ifndef NCC_GB300_DEBUG_H
+#define NCC_GB300_DEBUG_H
+
+#include "ncc.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * ncc_debug_set_fault -- test hook for the bounded waits.  While
+ * suppress_tile >= 0, the SAT builder's tile with that row-major index never
+ * publishes its look-back results, so every tile that depends on it waits
+ * until its limit (timeout_ns; 0 restores the default of one second) runs
+ * out and records NCC_ERR_TIMEOUT.  suppress_tile = -1 restores normal
+ * operation.  Process-wide; not for concurrent use.
+ */
+int ncc_debug_set_fault(int suppress_tile, uint64_t timeout_ns);
+
+/*
+ * ncc_debug_fail_alloc -- test hook for allocation failure.  The next
+ * `count` device allocations the library makes (the SAT builder's look-back
+ * workspace when it is first allocated or grown, the host-buffer path's
+ * device buffers) fail as on an exhausted device, so the calls that need
+ * them return NCC_ERR_NOMEM and launch nothing.  count = 0 cancels the
+ * failures still pending.  Process-wide; not for concurrent use.
+ * Returns NCC_OK, or NCC_ERR_INVALID_ARG for a negative count.
+ */
+int ncc_debug_fail_alloc(int count);
+
+/* Kernels a correlate call can launch (ncc_debug_last_path). */
+enum ncc_path_code {
+    NCC_PATH_NONE = 0,
+    NCC_PATH_DP4A = 1,     /* single template, integer dot products         */
+    NCC_PATH_TENSOR = 2,   /* single template, tcgen05 tensor cores          */
+    NCC_PATH_BANK = 3      /* template bank, tcgen05 tensor cores            */
+};
+
+/*
+ * ncc_debug_set_path -- selects the single-template kernel that
+ * ncc_correlate, ncc_correlate_moments and ncc_correlate_bank (for banks the
+ * bank kernel does not take) use.  0 = automatic (dp4a), NCC_PATH_DP4A =
+ * dp4a, NCC_PATH_TENSOR = tensor cores (NCC_ERR_UNSUPPORTED where they do not
+ * apply).  Process-wide; not for concurrent use.
+ * Returns NCC_OK, or NCC_ERR_INVALID_ARG for another value.
+ */
+int ncc_debug_set_path(int path);
+
+/*
+ * ncc_debug_last_path -- the kernel (ncc_path_code) launched by the most
+ * recent successful correlate call of this process; NCC_PATH_NONE before
+ * the first.
+ */
+int ncc_debug_last_path(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NCC_GB300_DEBUG_H */

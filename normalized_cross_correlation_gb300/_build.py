@@ -37,7 +37,7 @@ def _sources() -> list[str]:
 
 def _deps() -> list[str]:
     return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + \
-        [os.path.join(INCLUDE, "ncc.h"), os.path.abspath(__file__)]
+        sorted(glob.glob(os.path.join(INCLUDE, "*.h"))) + [os.path.abspath(__file__)]
 
 
 def up_to_date() -> bool:

@@ -1,8 +1,9 @@
-// ncc_api.cu -- the library's C ABI (declared in include/ncc.h): argument
-// checks, stream-ordered workspace, kernel selection and the per-device
-// status word.
+// ncc_api.cu -- the library's C ABI (declared in include/ncc.h, the test
+// hooks in include/ncc_debug.h): argument checks, the stream-ordered device
+// memory pool, kernel selection and the per-device status word.
 #include "ncc_common.cuh"
 
+#include <atomic>
 #include <mutex>
 #include <string.h>
 
@@ -10,16 +11,31 @@ namespace {
 
 // Per-device status word written by kernels (first error wins).
 __device__ int g_ncc_status = 0;
+// Where ncc_sync_status's read-and-clear kernel leaves the word it took.
+__device__ int g_ncc_status_taken = 0;
+
+// Takes the status word and leaves zero in one atomic step, so an error
+// recorded at any moment is either returned now or kept for the next call.
+__global__ void take_status_kernel(int *status, int *taken) { *taken = atomicExch(status, 0); }
 
 constexpr int kMaxDevices = 64;
 int *g_status_ptr[kMaxDevices] = {};
 std::mutex g_mutex;
 
-// Test hook state (ncc_debug_set_fault, ncc_debug_set_path).
+// Test hook state (ncc_debug_set_fault, ncc_debug_set_path,
+// ncc_debug_fail_alloc), guarded by g_mutex except the failure count.
 int g_fault_tile = -1;
 uint64_t g_timeout_ns = 1000000000ull;
 int g_path = 0;
 int g_last_path = NCC_PATH_NONE;
+std::atomic<int> g_fail_allocs{0};
+std::mutex g_take_mutex;  // one read-and-clear at a time (shared landing word)
+int *g_taken_ptr[kMaxDevices] = {};
+
+void set_last_path(int path) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_last_path = path;
+}
 
 constexpr int kMaxW = 66051;  // 66051 * 255^2 < 2^32: a row's running sum of squares fits uint32
 constexpr long long kMaxN = 66051;  // wT*hT*255^2 < 2^32: SumIT fits uint32
@@ -61,10 +77,11 @@ int check_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int w
     return NCC_OK;
 }
 
-// Stream-ordered pool for the host-buffer path's device buffers, one per
-// device.  Its release threshold keeps freed memory reserved, so repeated
-// calls reuse it instead of mapping it afresh after every synchronization
-// (what the default pool, which releases at each synchronization, would do).
+// Stream-ordered pool for the library's device memory (the SAT builder's
+// look-back workspace, the host-buffer path's buffers), one per device.  Its
+// release threshold keeps freed memory reserved, so repeated calls reuse it
+// instead of mapping it afresh after every synchronization (what the default
+// pool, which releases at each synchronization, would do).
 cudaMemPool_t g_host_pool[kMaxDevices] = {};
 
 int host_path_pool(cudaMemPool_t *out) {
@@ -128,7 +145,7 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
     if (!direct && nT > 1 && ncc::bank_tc_supported(W, H, wT, hT, nT)) {
         ncc::BankArgs b{img, W, H, tmpl, wT, hT, nT, S, Q, out, sumI, sumI2, sumIT, status};
         rc = to_status(ncc::bank_tc_launch(b, stream));
-        if (rc == NCC_OK) g_last_path = NCC_PATH_BANK;
+        if (rc == NCC_OK) set_last_path(NCC_PATH_BANK);
         return rc;
     }
     if (direct) path = NCC_PATH_DP4A;  // the direct moments exist on the dp4a kernel only
@@ -164,7 +181,7 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
         }
         if (e != cudaSuccess) return to_status(e);
     }
-    g_last_path = used;
+    set_last_path(used);
     return NCC_OK;
 }
 
@@ -174,6 +191,17 @@ namespace ncc {
 // The per-device status word's device address, for entry points defined in
 // other translation units.
 int status_word(int **out) { return status_ptr(out); }
+
+cudaError_t pool_alloc(void **ptr, size_t bytes, cudaStream_t stream) {
+    int left = g_fail_allocs.load();
+    while (left > 0) {
+        if (g_fail_allocs.compare_exchange_weak(left, left - 1)) return cudaErrorMemoryAllocation;
+    }
+    cudaMemPool_t pool = nullptr;
+    const int rc = host_path_pool(&pool);
+    if (rc != NCC_OK) return cudaErrorInitializationError;
+    return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+}
 }  // namespace ncc
 
 extern "C" {
@@ -335,11 +363,8 @@ int ncc_match_host(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT
     const size_t outBytes = direct ? 0 : nout * 4;
     const size_t offQ = n * 8, offOut = 2 * n * 8, offImg = (offOut + outBytes + 255) / 256 * 256;
     const size_t offT = (offImg + n + 255) / 256 * 256, total = offT + nt;
-    cudaMemPool_t pool = nullptr;
-    rc = host_path_pool(&pool);
-    if (rc != NCC_OK) return rc;
     char *d = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&d), total, pool, st);
+    cudaError_t e = ncc::pool_alloc(reinterpret_cast<void **>(&d), total, st);
     if (e != cudaSuccess) return e == cudaErrorMemoryAllocation ? NCC_ERR_NOMEM : NCC_ERR_CUDA;
     int64_t *S = reinterpret_cast<int64_t *>(d), *Q = reinterpret_cast<int64_t *>(d + offQ);
     float *dout = direct ? direct : reinterpret_cast<float *>(d + offOut);
@@ -358,19 +383,28 @@ int ncc_match_host(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT
 }
 
 int ncc_sync_status(ncc_stream_t stream) {
-    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return NCC_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return NCC_ERR_CUDA;
     int *status = nullptr;
     int rc = status_ptr(&status);
     if (rc != NCC_OK) return rc;
-    int v = 0;
-    if (cudaMemcpy(&v, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-        return NCC_ERR_CUDA;
-    if (v != 0) {
-        const int zero = 0;
-        if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
-            return NCC_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NCC_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_take_mutex);
+    if (!g_taken_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ncc_status_taken) != cudaSuccess) return NCC_ERR_CUDA;
+        g_taken_ptr[dev] = static_cast<int *>(p);
     }
+    // read and clear in one atomic exchange on the device, then fetch the
+    // value it took; both in stream order after the work just synchronized
+    take_status_kernel<<<1, 1, 0, st>>>(status, g_taken_ptr[dev]);
+    if (cudaGetLastError() != cudaSuccess) return NCC_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyAsync(&v, g_taken_ptr[dev], sizeof(int), cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return NCC_ERR_CUDA;
     return v;
 }
 
@@ -395,7 +429,16 @@ int ncc_debug_set_path(int path) {
     return NCC_OK;
 }
 
-int ncc_debug_last_path(void) { return g_last_path; }
+int ncc_debug_last_path(void) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    return g_last_path;
+}
+
+int ncc_debug_fail_alloc(int count) {
+    if (count < 0) return NCC_ERR_INVALID_ARG;
+    g_fail_allocs.store(count);
+    return NCC_OK;
+}
 
 int ncc_debug_set_fault(int suppress_tile, uint64_t timeout_ns) {
     if (suppress_tile < -1) return NCC_ERR_INVALID_ARG;

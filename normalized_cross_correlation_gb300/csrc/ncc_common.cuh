@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include "../../include/ncc.h"
+#include "../../include/ncc_debug.h"
 
 namespace ncc {
 
@@ -108,6 +109,16 @@ inline bool make_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType type, int e
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// ---------------------------------------------------------------------------
+// Library-owned device memory (defined in ncc_api.cu).
+// ---------------------------------------------------------------------------
+
+// Stream-ordered allocation from the library's per-device pool, whose
+// release threshold keeps freed memory reserved for the next request.  While
+// the allocation-failure test hook (ncc_debug_fail_alloc) has failures left,
+// it fails with cudaErrorMemoryAllocation as an exhausted device would.
+cudaError_t pool_alloc(void **ptr, size_t bytes, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Host launchers (defined in the kernel translation units).

@@ -694,7 +694,9 @@ constexpr size_t kHeaderBytes = 256 + kMaxSmIds * sizeof(unsigned);
 static_assert(kHeaderBytes % 256 == 0, "row words stay 256-byte aligned");
 
 // Library-owned look-back workspace, one per device.  Calls on different
-// streams are ordered through `last` so they never use it concurrently.
+// streams are ordered through `last` so they never use it concurrently; it
+// is allocated, grown and cleared in stream order, without a host
+// synchronization.
 struct DeviceWs {
     void *ptr = nullptr;
     size_t bytes = 0;
@@ -813,15 +815,25 @@ cudaError_t sat_build_run(const uint8_t *img, int W, int H, int64_t *S, int64_t 
     }
     if (d.bytes < plan.total_bytes) {
         if (d.ptr) {
-            if (d.used) cudaEventSynchronize(d.last);
-            cudaFree(d.ptr);
+            // the old workspace goes back to the pool after its last use:
+            // order this stream after that use, then free in stream order
+            if (d.used && d.last_stream != stream) {
+                e = cudaStreamWaitEvent(stream, d.last, 0);
+                if (e != cudaSuccess) return e;
+            }
+            e = cudaFreeAsync(d.ptr, stream);
+            if (e != cudaSuccess) return e;
             d.ptr = nullptr;
             d.bytes = 0;
+            d.used = false;
         }
         const size_t bytes = align_up(plan.total_bytes, 1 << 20);
-        e = cudaMalloc(&d.ptr, bytes);
-        if (e != cudaSuccess) return e;
-        e = cudaMemset(d.ptr, 0, bytes);
+        e = pool_alloc(&d.ptr, bytes, stream);
+        if (e != cudaSuccess) {
+            d.ptr = nullptr;
+            return e;
+        }
+        e = cudaMemsetAsync(d.ptr, 0, bytes, stream);
         if (e != cudaSuccess) return e;
         d.bytes = bytes;
         d.epoch = 0;

@@ -2,11 +2,10 @@
 // builder for callers that must not allocate device memory.
 //
 // Who needs it: code that runs where a cudaMalloc is not allowed or not
-// wanted -- inside a CUDA stream capture (allocation calls are not
-// capturable), inside a host callback or a real-time loop that must not
-// block (cudaMalloc and cudaFree can synchronize the device), or inside a
-// host framework that owns all device memory through its own pool and
-// budget, where a hidden allocation would fail or fragment it.  The regular
+// wanted -- a host callback or a real-time loop that must not block
+// (cudaMalloc and cudaFree can synchronize the whole device), or a host
+// framework that owns all device memory through its own pool and budget,
+// where a hidden allocation would fail or fragment it.  The regular
 // ncc_sat_build allocates its look-back workspace on first use; this entry
 // point instead uses a fixed scratch array compiled into the library.
 //

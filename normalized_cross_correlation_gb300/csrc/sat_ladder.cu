@@ -36,32 +36,35 @@ constexpr uint64_t kValueMask = (1ull << kStateShift) - 1;
 
 // ---------------------------------------------------------------- naive --
 
-__global__ void naive_rows_kernel(const uint8_t *__restrict__ img, int W, int H,
+// The one-thread-per-line build of section 15.8: each thread owns one line
+// of the tables and walks it from its first element to its last, replacing
+// every element by the running total of the line so far, for S and Q in the
+// same walk.  The build is two launches of this kernel.  Along rows the
+// values walked are the pixels and their squares; along columns they are
+// what the row launch left in S and Q, so after the column launch every
+// element holds its whole upper-left rectangle.  Rows are walked with unit
+// stride but the threads of a warp sit W elements apart, so that launch is
+// uncoalesced by construction -- the cost the section measures.
+template <bool kAlongRows>
+__global__ void naive_line_kernel(const uint8_t *__restrict__ img, int W, int H,
                                   long long *__restrict__ S, long long *__restrict__ Q) {
-    const int y = blockIdx.x * blockDim.x + threadIdx.x;
-    if (y >= H) return;
-    const uint8_t *row = img + (size_t)y * W;
-    long long *sr = S + (size_t)y * W, *qr = Q + (size_t)y * W;
-    long long s = 0, q = 0;
-    for (int x = 0; x < W; ++x) {
-        const int v = row[x];
-        s += v;
-        q += v * v;
-        sr[x] = s;
-        qr[x] = q;
-    }
-}
-
-__global__ void naive_cols_kernel(int W, int H, long long *__restrict__ S, long long *__restrict__ Q) {
-    const int x = blockIdx.x * blockDim.x + threadIdx.x;
-    if (x >= W) return;
-    long long s = 0, q = 0;
-    for (int y = 0; y < H; ++y) {
-        const size_t o = (size_t)y * W + x;
-        s += S[o];
-        q += Q[o];
-        S[o] = s;
-        Q[o] = q;
+    const int line = blockIdx.x * blockDim.x + threadIdx.x;
+    if (line >= (kAlongRows ? H : W)) return;
+    const size_t step = kAlongRows ? 1 : (size_t)W;
+    const size_t begin = kAlongRows ? (size_t)line * W : (size_t)line;
+    const size_t end = begin + step * (size_t)(kAlongRows ? W : H);
+    long long total = 0, total_sq = 0;
+    for (size_t o = begin; o != end; o += step) {
+        if constexpr (kAlongRows) {
+            const long long v = img[o];
+            total += v;
+            total_sq += v * v;
+        } else {
+            total += S[o];
+            total_sq += Q[o];
+        }
+        S[o] = total;
+        Q[o] = total_sq;
     }
 }
 
@@ -216,10 +219,10 @@ cudaError_t sat_ladder_run(int variant, const uint8_t *img, int W, int H, int64_
                            int *status, uint64_t timeout_ns, cudaStream_t stream) {
     long long *s = reinterpret_cast<long long *>(S), *q = reinterpret_cast<long long *>(Q);
     if (variant == NCC_SAT_NAIVE) {
-        naive_rows_kernel<<<(H + 127) / 128, 128, 0, stream>>>(img, W, H, s, q);
+        naive_line_kernel<true><<<(H + 127) / 128, 128, 0, stream>>>(img, W, H, s, q);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        naive_cols_kernel<<<(W + 127) / 128, 128, 0, stream>>>(W, H, s, q);
+        naive_line_kernel<false><<<(W + 127) / 128, 128, 0, stream>>>(img, W, H, s, q);
         return cudaGetLastError();
     }
     if (variant != NCC_SAT_TWO_PASS) return cudaErrorInvalidValue;

@@ -29,7 +29,8 @@ NCC_SAT_TWO_PASS = 2   # uint32 row sums, then a column look-back scan
 EXPORTS = ("ncc_sat_build", "ncc_sat_build_noalloc", "ncc_sat_build_variant", "ncc_correlate", "ncc_correlate_bank", "ncc_correlate_moments",
            "ncc_correlate_direct", "ncc_correlate_direct_moments",
            "ncc_match", "ncc_match_host", "ncc_sync_status", "ncc_status_string", "ncc_version",
-           "ncc_debug_set_fault", "ncc_debug_set_path", "ncc_debug_last_path")
+           "ncc_debug_set_fault", "ncc_debug_fail_alloc", "ncc_debug_set_path",
+           "ncc_debug_last_path")
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +73,7 @@ def lib() -> ctypes.CDLL:
             L.ncc_status_string.restype = ctypes.c_char_p
             L.ncc_version.argtypes = []
             L.ncc_debug_set_fault.argtypes = [i, u64]
+            L.ncc_debug_fail_alloc.argtypes = [i]
             L.ncc_debug_set_path.argtypes = [i]
             L.ncc_debug_last_path.argtypes = []
             for name in EXPORTS:
@@ -100,13 +102,32 @@ def _stream_handle(stream) -> int:
     return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _dev(t, dtype, ndim: int, name: str):
+def _dev(t, dtype, ndim: int, name: str, like=None, shape=None):
+    """Checks that t is a contiguous CUDA tensor of the given dtype and rank,
+    on the same device as `like` and of exactly `shape` when those are given,
+    so that no kernel is handed a buffer it would read or write past."""
     import torch
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype or t.dim() != ndim or not t.is_contiguous():
         raise TypeError(f"{name} must be a contiguous {dtype} tensor with {ndim} dims")
+    if like is not None and t.device != like.device:
+        raise ValueError(f"{name} is on {t.device}, the image on {like.device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
     return t
+
+
+def _tables(img, S, Q):
+    """Caller tables: int64 [H][W] on the image's device."""
+    import torch
+    _dev(S, torch.int64, 2, "S", img, img.shape)
+    _dev(Q, torch.int64, 2, "Q", img, img.shape)
+
+
+def _map_shape(img, nT, hT, wT):
+    H, W = img.shape
+    return (nT, max(H - hT + 1, 0), max(W - wT + 1, 0))
 
 
 def _tmpl3(t):
@@ -117,17 +138,21 @@ def _tmpl3(t):
 # Entry points (C names).
 # --------------------------------------------------------------------------
 
+def _new_tables(img):
+    import torch
+    return (torch.empty(tuple(img.shape), dtype=torch.int64, device=img.device),
+            torch.empty(tuple(img.shape), dtype=torch.int64, device=img.device))
+
+
 def ncc_sat_build(img, S=None, Q=None, stream=None):
     """S = SAT(I), Q = SAT(I^2): inclusive int64 tables of a uint8 [H][W] image."""
     import torch
     _dev(img, torch.uint8, 2, "img")
     H, W = img.shape
-    if S is None:
-        S = torch.empty((H, W), dtype=torch.int64, device=img.device)
-    if Q is None:
-        Q = torch.empty((H, W), dtype=torch.int64, device=img.device)
-    _dev(S, torch.int64, 2, "S")
-    _dev(Q, torch.int64, 2, "Q")
+    nS, nQ = _new_tables(img) if S is None or Q is None else (S, Q)
+    S = nS if S is None else S
+    Q = nQ if Q is None else Q
+    _tables(img, S, Q)
     _check(lib().ncc_sat_build(img.data_ptr(), W, H, S.data_ptr(), Q.data_ptr(),
                                _stream_handle(stream)), "ncc_sat_build")
     return S, Q
@@ -139,14 +164,13 @@ def ncc_sat_build_variant(img, variant, S=None, Q=None, stream=None):
     import torch
     _dev(img, torch.uint8, 2, "img")
     H, W = img.shape
-    if S is None:
-        S = torch.empty((H, W), dtype=torch.int64, device=img.device)
-    if Q is None:
-        Q = torch.empty((H, W), dtype=torch.int64, device=img.device)
-    _dev(S, torch.int64, 2, "S")
-    _dev(Q, torch.int64, 2, "Q")
-    _check(lib().ncc_sat_build_variant(img.data_ptr(), W, H, S.data_ptr(), Q.data_ptr(), int(variant),
-                                       _stream_handle(stream)), "ncc_sat_build_variant")
+    nS, nQ = _new_tables(img) if S is None or Q is None else (S, Q)
+    S = nS if S is None else S
+    Q = nQ if Q is None else Q
+    _tables(img, S, Q)
+    _check(lib().ncc_sat_build_variant(img.data_ptr(), W, H, S.data_ptr(), Q.data_ptr(),
+                                       int(variant), _stream_handle(stream)),
+           "ncc_sat_build_variant")
     return S, Q
 
 
@@ -155,8 +179,7 @@ def ncc_sat_build_noalloc(img, S, Q, stream=None):
     (int64 [H][W]); for callers that cannot allocate (see include/ncc.h)."""
     import torch
     _dev(img, torch.uint8, 2, "img")
-    _dev(S, torch.int64, 2, "S")
-    _dev(Q, torch.int64, 2, "Q")
+    _tables(img, S, Q)
     H, W = img.shape
     _check(lib().ncc_sat_build_noalloc(img.data_ptr(), W, H, S.data_ptr(), Q.data_ptr(),
                                        _stream_handle(stream)), "ncc_sat_build_noalloc")
@@ -167,13 +190,14 @@ def ncc_correlate(img, tmpl, S, Q, out=None, stream=None):
     """fp32 [Oy][Ox] coefficients of one uint8 [hT][wT] template."""
     import torch
     _dev(img, torch.uint8, 2, "img")
-    _dev(tmpl, torch.uint8, 2, "tmpl")
+    _dev(tmpl, torch.uint8, 2, "tmpl", img)
+    _tables(img, S, Q)
     H, W = img.shape
     hT, wT = tmpl.shape
+    shape = _map_shape(img, 1, hT, wT)[1:]
     if out is None:
-        out = torch.empty((max(H - hT + 1, 0), max(W - wT + 1, 0)), dtype=torch.float32,
-                          device=img.device)
-    _dev(out, torch.float32, 2, "out")
+        out = torch.empty(shape, dtype=torch.float32, device=img.device)
+    _dev(out, torch.float32, 2, "out", img, shape)
     _check(lib().ncc_correlate(img.data_ptr(), W, H, tmpl.data_ptr(), wT, hT, S.data_ptr(),
                                Q.data_ptr(), out.data_ptr(), _stream_handle(stream)),
            "ncc_correlate")
@@ -185,17 +209,26 @@ def ncc_correlate_bank(img, tmpls, S, Q, out=None, stream=None):
     import torch
     _dev(img, torch.uint8, 2, "img")
     tmpls = _tmpl3(tmpls)
-    _dev(tmpls, torch.uint8, 3, "tmpls")
+    _dev(tmpls, torch.uint8, 3, "tmpls", img)
+    _tables(img, S, Q)
     H, W = img.shape
     nT, hT, wT = tmpls.shape
+    shape = _map_shape(img, nT, hT, wT)
     if out is None:
-        out = torch.empty((nT, max(H - hT + 1, 0), max(W - wT + 1, 0)), dtype=torch.float32,
-                          device=img.device)
-    _dev(out, torch.float32, 3, "out")
+        out = torch.empty(shape, dtype=torch.float32, device=img.device)
+    _dev(out, torch.float32, 3, "out", img, shape)
     _check(lib().ncc_correlate_bank(img.data_ptr(), W, H, tmpls.data_ptr(), wT, hT, nT,
                                     S.data_ptr(), Q.data_ptr(), out.data_ptr(),
                                     _stream_handle(stream)), "ncc_correlate_bank")
     return out
+
+
+def _moment_buffers(img, nT, hT, wT):
+    import torch
+    shape = _map_shape(img, nT, hT, wT)
+    return (torch.empty(shape[1:], dtype=torch.int64, device=img.device),
+            torch.empty(shape[1:], dtype=torch.int64, device=img.device),
+            torch.empty(shape, dtype=torch.int64, device=img.device))
 
 
 def ncc_correlate_moments(img, tmpls, S, Q, stream=None):
@@ -203,13 +236,11 @@ def ncc_correlate_moments(img, tmpls, S, Q, stream=None):
     import torch
     _dev(img, torch.uint8, 2, "img")
     tmpls = _tmpl3(tmpls)
-    _dev(tmpls, torch.uint8, 3, "tmpls")
+    _dev(tmpls, torch.uint8, 3, "tmpls", img)
+    _tables(img, S, Q)
     H, W = img.shape
     nT, hT, wT = tmpls.shape
-    Oy, Ox = max(H - hT + 1, 0), max(W - wT + 1, 0)
-    sI = torch.empty((Oy, Ox), dtype=torch.int64, device=img.device)
-    sI2 = torch.empty((Oy, Ox), dtype=torch.int64, device=img.device)
-    sIT = torch.empty((nT, Oy, Ox), dtype=torch.int64, device=img.device)
+    sI, sI2, sIT = _moment_buffers(img, nT, hT, wT)
     _check(lib().ncc_correlate_moments(img.data_ptr(), W, H, tmpls.data_ptr(), wT, hT, nT,
                                        S.data_ptr(), Q.data_ptr(), sI.data_ptr(),
                                        sI2.data_ptr(), sIT.data_ptr(), _stream_handle(stream)),
@@ -223,13 +254,13 @@ def ncc_correlate_direct(img, tmpls, out=None, stream=None):
     import torch
     _dev(img, torch.uint8, 2, "img")
     tmpls = _tmpl3(tmpls)
-    _dev(tmpls, torch.uint8, 3, "tmpls")
+    _dev(tmpls, torch.uint8, 3, "tmpls", img)
     H, W = img.shape
     nT, hT, wT = tmpls.shape
+    shape = _map_shape(img, nT, hT, wT)
     if out is None:
-        out = torch.empty((nT, max(H - hT + 1, 0), max(W - wT + 1, 0)), dtype=torch.float32,
-                          device=img.device)
-    _dev(out, torch.float32, 3, "out")
+        out = torch.empty(shape, dtype=torch.float32, device=img.device)
+    _dev(out, torch.float32, 3, "out", img, shape)
     _check(lib().ncc_correlate_direct(img.data_ptr(), W, H, tmpls.data_ptr(), wT, hT, nT,
                                       out.data_ptr(), _stream_handle(stream)),
            "ncc_correlate_direct")
@@ -242,13 +273,10 @@ def ncc_correlate_direct_moments(img, tmpls, stream=None):
     import torch
     _dev(img, torch.uint8, 2, "img")
     tmpls = _tmpl3(tmpls)
-    _dev(tmpls, torch.uint8, 3, "tmpls")
+    _dev(tmpls, torch.uint8, 3, "tmpls", img)
     H, W = img.shape
     nT, hT, wT = tmpls.shape
-    Oy, Ox = max(H - hT + 1, 0), max(W - wT + 1, 0)
-    sI = torch.empty((Oy, Ox), dtype=torch.int64, device=img.device)
-    sI2 = torch.empty((Oy, Ox), dtype=torch.int64, device=img.device)
-    sIT = torch.empty((nT, Oy, Ox), dtype=torch.int64, device=img.device)
+    sI, sI2, sIT = _moment_buffers(img, nT, hT, wT)
     _check(lib().ncc_correlate_direct_moments(img.data_ptr(), W, H, tmpls.data_ptr(), wT, hT, nT,
                                               sI.data_ptr(), sI2.data_ptr(), sIT.data_ptr(),
                                               _stream_handle(stream)),
@@ -263,19 +291,17 @@ def ncc_match(img, tmpls, S=None, Q=None, out=None, stream=None):
     import torch
     _dev(img, torch.uint8, 2, "img")
     tmpls = _tmpl3(tmpls)
-    _dev(tmpls, torch.uint8, 3, "tmpls")
+    _dev(tmpls, torch.uint8, 3, "tmpls", img)
     H, W = img.shape
     nT, hT, wT = tmpls.shape
-    if S is None:
-        S = torch.empty((H, W), dtype=torch.int64, device=img.device)
-    if Q is None:
-        Q = torch.empty((H, W), dtype=torch.int64, device=img.device)
-    _dev(S, torch.int64, 2, "S")
-    _dev(Q, torch.int64, 2, "Q")
+    nS, nQ = _new_tables(img) if S is None or Q is None else (S, Q)
+    S = nS if S is None else S
+    Q = nQ if Q is None else Q
+    _tables(img, S, Q)
+    shape = _map_shape(img, nT, hT, wT)
     if out is None:
-        out = torch.empty((nT, max(H - hT + 1, 0), max(W - wT + 1, 0)), dtype=torch.float32,
-                          device=img.device)
-    _dev(out, torch.float32, 3, "out")
+        out = torch.empty(shape, dtype=torch.float32, device=img.device)
+    _dev(out, torch.float32, 3, "out", img, shape)
     _check(lib().ncc_match(img.data_ptr(), W, H, tmpls.data_ptr(), wT, hT, nT, S.data_ptr(),
                            Q.data_ptr(), out.data_ptr(), _stream_handle(stream)), "ncc_match")
     return S, Q, out
@@ -285,24 +311,35 @@ def ncc_match_host(img, tmpls, out=None, stream=None):
     """The whole path on HOST buffers (numpy arrays or CPU tensors; pinned
     tensors make the copies asynchronous).  Returns fp32 [nT][Oy][Ox] on the
     host; synchronizes the stream."""
-    def host_ptr(a):
-        if isinstance(a, np.ndarray):
-            if not a.flags.c_contiguous:
-                raise TypeError("host arrays must be C-contiguous")
-            return a.ctypes.data, a.shape
-        if a.is_cuda or not a.is_contiguous():
-            raise TypeError("host tensors must be contiguous CPU tensors")
-        return a.data_ptr(), tuple(a.shape)
+    import torch
+    kinds = {"uint8": (np.uint8, torch.uint8), "float32": (np.float32, torch.float32)}
 
-    ip, ishape = host_ptr(img)
+    def host_ptr(a, kind, ndim, name, shape=None):
+        np_t, torch_t = kinds[kind]
+        if isinstance(a, np.ndarray):
+            if not a.flags.c_contiguous or a.dtype != np_t or a.ndim != ndim:
+                raise TypeError(f"{name} must be a C-contiguous {kind} array with {ndim} dims")
+            dims = tuple(a.shape)
+            ptr = a.ctypes.data
+        elif isinstance(a, torch.Tensor):
+            if a.is_cuda or not a.is_contiguous() or a.dtype != torch_t or a.dim() != ndim:
+                raise TypeError(f"{name} must be a contiguous CPU {kind} tensor with {ndim} dims")
+            dims = tuple(a.shape)
+            ptr = a.data_ptr()
+        else:
+            raise TypeError(f"{name} must be a numpy array or a CPU tensor")
+        if shape is not None and dims != tuple(shape):
+            raise ValueError(f"{name} has shape {dims}, expected {tuple(shape)}")
+        return ptr, dims
+
+    ip, (H, W) = host_ptr(img, "uint8", 2, "img")
     if len(tmpls.shape) == 2:
         tmpls = tmpls.reshape((1,) + tuple(tmpls.shape))
-    tp, tshape = host_ptr(tmpls)
-    H, W = ishape
-    nT, hT, wT = tshape
+    tp, (nT, hT, wT) = host_ptr(tmpls, "uint8", 3, "tmpls")
+    shape = (nT, max(H - hT + 1, 0), max(W - wT + 1, 0))
     if out is None:
-        out = np.empty((nT, H - hT + 1, W - wT + 1), np.float32)
-    op, _ = host_ptr(out)
+        out = np.empty(shape, np.float32)
+    op, _ = host_ptr(out, "float32", 3, "out", shape)
     _check(lib().ncc_match_host(ip, W, H, tp, wT, hT, nT, op, _stream_handle(stream)),
            "ncc_match_host")
     return out
@@ -322,6 +359,11 @@ def ncc_version() -> int:
 
 def ncc_debug_set_fault(suppress_tile: int, timeout_ns: int = 0) -> None:
     _check(lib().ncc_debug_set_fault(int(suppress_tile), int(timeout_ns)), "ncc_debug_set_fault")
+
+
+def ncc_debug_fail_alloc(count: int) -> None:
+    """The library's next `count` device allocations fail (NCC_ERR_NOMEM)."""
+    _check(lib().ncc_debug_fail_alloc(int(count)), "ncc_debug_fail_alloc")
 
 
 NCC_PATH_NONE, NCC_PATH_DP4A, NCC_PATH_TENSOR, NCC_PATH_BANK = 0, 1, 2, 3

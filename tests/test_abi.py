@@ -1,5 +1,5 @@
 """The C-ABI library builds, loads without a GPU and exports every entry
-point include/ncc.h declares; argument checks answer before any CUDA call."""
+point include/*.h declares; argument checks answer before any CUDA call."""
 import ctypes
 import os
 import re
@@ -10,7 +10,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def declared_functions():
-    src = open(os.path.join(ROOT, "include", "ncc.h")).read()
+    inc = os.path.join(ROOT, "include")
+    src = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc))
+                  if f.endswith(".h"))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(ncc_[a-z_]+)\s*\(", src)))
 
@@ -96,6 +98,8 @@ def test_argument_checks_need_no_gpu(built_lib):
         assert L.ncc_sat_build_variant(fake, 66052, 1, fake * 4, fake * 8, v, None) == ncc.NCC_ERR_UNSUPPORTED
         assert L.ncc_sat_build_variant(fake, 16, 16, fake * 4, fake * 4 + 8, v, None) == ncc.NCC_ERR_INVALID_ARG
     assert L.ncc_debug_set_fault(-2, 0) == ncc.NCC_ERR_INVALID_ARG
+    assert L.ncc_debug_fail_alloc(-1) == ncc.NCC_ERR_INVALID_ARG
+    assert L.ncc_debug_fail_alloc(0) == ncc.NCC_OK
 
 
 def test_product_path_does_not_import_the_oracle():
@@ -131,8 +135,31 @@ def test_binding_refuses_cpu_tensors():
             call()
 
 
+def test_host_entry_point_checks_dtypes_and_output_shape(monkeypatch):
+    """ncc_match_host refuses host buffers of the wrong dtype, layout or
+    output shape before it calls the library."""
+    import numpy as np
+    from normalized_cross_correlation_gb300 import ncc
+
+    def refuse():
+        raise AssertionError("the binding reached the library with bad arguments")
+    monkeypatch.setattr(ncc, "lib", refuse)
+    img = np.zeros((64, 80), np.uint8)
+    T = np.zeros((1, 8, 6), np.uint8)
+    refused = [
+        lambda: ncc.ncc_match_host(img.astype(np.int16), T),
+        lambda: ncc.ncc_match_host(img, T.astype(np.float32)),
+        lambda: ncc.ncc_match_host(img, T, out=np.zeros((1, 57, 74), np.float32)),
+        lambda: ncc.ncc_match_host(img, T, out=np.zeros((1, 57, 75), np.float64)),
+        lambda: ncc.ncc_match_host(img[:, ::2], T),
+    ]
+    for call in refused:
+        with pytest.raises((TypeError, ValueError)):
+            call()
+
+
 def test_header_is_plain_c_and_links(built_lib, tmp_path):
-    """include/ncc.h compiles as strict C99 (no C++ or CUDA headers needed),
+    """include/ncc.h and ncc_debug.h compile as strict C99 (no C++ or CUDA headers needed),
     and a C program links against the library and calls it without a GPU."""
     import shutil
     import subprocess
@@ -142,6 +169,7 @@ def test_header_is_plain_c_and_links(built_lib, tmp_path):
     src = tmp_path / "use_ncc.c"
     src.write_text(
         '#include "ncc.h"\n'
+        '#include "ncc_debug.h"\n'
         "int main(void) {\n"
         "    if (ncc_version() <= 0) return 1;\n"
         "    if (ncc_sat_build(0, 16, 16, 0, 0, 0) != NCC_ERR_INVALID_ARG) return 2;\n"

@@ -3,13 +3,15 @@
 Integers (SumI, SumI2, SumIT) must match bit-exactly; coefficients within
 1e-5 absolute (the fp32 result against the oracle's double).  Sizes span
 several output tiles (128 x 32) with ragged tails; the full-size workloads
-compare every coefficient or, where the oracle would take minutes, whole
-sampled rows plus random shifts, in the launch configuration the bench uses.
+compare every coefficient (the largest ones in test_config_parity_gpu.py),
+in the launch configuration the bench uses.  Every output is written over a
+NaN-filled buffer, so a skipped cell fails.
 """
 import numpy as np
 import pytest
 
 import oracle
+from gpu_util import moments, nan_map, to_dev
 from normalized_cross_correlation_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -17,15 +19,12 @@ pytestmark = pytest.mark.gpu
 TOL = 1e-5
 
 
-def to_dev(a):
-    import torch
-    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
-
-
 def gpu_ncc(ncc, img, T):
+    """Coefficients of one template, written over a NaN-filled map."""
     dimg = to_dev(img)
     S, Q = ncc.ncc_sat_build(dimg)
-    r = ncc.ncc_correlate(dimg, to_dev(T), S, Q)
+    out = nan_map(img.shape[0] - T.shape[0] + 1, img.shape[1] - T.shape[1] + 1)
+    r = ncc.ncc_correlate(dimg, to_dev(T), S, Q, out=out)
     assert ncc.ncc_sync_status() == 0
     return r.cpu().numpy()
 
@@ -33,8 +32,7 @@ def gpu_ncc(ncc, img, T):
 def gpu_moments(ncc, img, T):
     dimg = to_dev(img)
     S, Q = ncc.ncc_sat_build(dimg)
-    sI, sI2, sIT = ncc.ncc_correlate_moments(dimg, to_dev(T), S, Q)
-    assert ncc.ncc_sync_status() == 0
+    sI, sI2, sIT = moments(ncc, dimg, to_dev(T), S, Q)
     return sI.cpu().numpy(), sI2.cpu().numpy(), sIT.cpu().numpy()
 
 
@@ -97,25 +95,6 @@ def test_headline_4096_full_map(ncc, threads):
     np.testing.assert_allclose(r, ref, rtol=0, atol=TOL)
     _, x, y = w.crops[0]
     assert abs(r[y, x] - 1.0) <= TOL
-
-
-def test_large_8192_sampled(ncc, threads):
-    w = inputs.large_8192()
-    r = gpu_ncc(ncc, w.image, w.templates[0])
-    assert r.shape == (8129, 8129)
-    rng = np.random.default_rng(12)
-    rows = np.concatenate([[0, 6000, 8128], rng.integers(0, 8129, 5)])
-    for y in rows:
-        ys = np.full(8129, y)
-        xs = np.arange(8129)
-        ref = oracle.correlate_at(w.image, w.templates[0], xs, ys, threads=threads)
-        np.testing.assert_allclose(r[y], ref, rtol=0, atol=TOL)
-    xs = rng.integers(0, 8129, 20000)
-    ys = rng.integers(0, 8129, 20000)
-    ref = oracle.correlate_at(w.image, w.templates[0], xs, ys, threads=threads)
-    np.testing.assert_allclose(r[ys, xs], ref, rtol=0, atol=TOL)
-    assert abs(r[6000, 4000] - 1.0) <= TOL
-    assert np.all(np.abs(r) <= 1.0)
 
 
 def test_zero_variance_windows_and_templates(ncc):

@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 
 import oracle
+from gpu_util import moments, nan_map, to_dev
 from normalized_cross_correlation_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -27,16 +28,10 @@ CASES = [  # (W, H, wT, hT)
 ]
 
 
-def to_dev(a):
-    import torch
-    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
-
-
 @pytest.mark.parametrize("W,H,wT,hT", CASES)
 def test_direct_moments_bit_exact(ncc, threads, W, H, wT, hT):
     w = inputs.random_case(W * 13 + H, W, H, wT, hT, nT=1, n_crops=1)
-    sI, sI2, sIT = ncc.ncc_correlate_direct_moments(to_dev(w.image), to_dev(w.templates))
-    assert ncc.ncc_sync_status() == 0
+    sI, sI2, sIT = moments(ncc, to_dev(w.image), to_dev(w.templates), direct=True)
     _, oI, oI2, oIT = oracle.correlate(w.image, w.templates[0], with_sums=True, threads=threads)
     np.testing.assert_array_equal(sI.cpu().numpy(), oI)
     np.testing.assert_array_equal(sI2.cpu().numpy(), oI2)
@@ -47,9 +42,9 @@ def test_direct_moments_bit_exact(ncc, threads, W, H, wT, hT):
 def test_direct_coefficients_equal_the_table_path(ncc, threads, W, H, wT, hT):
     w = inputs.random_case(W * 19 + H, W, H, wT, hT, nT=1, n_crops=1)
     dimg, dt = to_dev(w.image), to_dev(w.templates)
-    r = ncc.ncc_correlate_direct(dimg, dt)
+    r = ncc.ncc_correlate_direct(dimg, dt, out=nan_map(1, w.Oy, w.Ox))
     S, Q = ncc.ncc_sat_build(dimg)
-    r0 = ncc.ncc_correlate(dimg, dt[0], S, Q)
+    r0 = ncc.ncc_correlate(dimg, dt[0], S, Q, out=nan_map(w.Oy, w.Ox))
     assert ncc.ncc_sync_status() == 0
     np.testing.assert_array_equal(r.cpu().numpy()[0], r0.cpu().numpy())
     ref = oracle.correlate(w.image, w.templates[0], threads=threads)
@@ -63,15 +58,16 @@ def test_direct_headline_4096_equals_the_table_path(ncc):
     """The bench's workload, in the launch configuration the bench times."""
     w = inputs.headline_4096()
     dimg, dt = to_dev(w.image), to_dev(w.templates)
-    r = ncc.ncc_correlate_direct(dimg, dt)
-    S, Q, r0 = ncc.ncc_match(dimg, dt)
+    r = ncc.ncc_correlate_direct(dimg, dt, out=nan_map(1, w.Oy, w.Ox))
+    S, Q, r0 = ncc.ncc_match(dimg, dt, out=nan_map(1, w.Oy, w.Ox))
     assert ncc.ncc_sync_status() == 0
     np.testing.assert_array_equal(r.cpu().numpy(), r0.cpu().numpy())
 
 
 def test_direct_bank_matches_oracle(ncc, threads):
     w = inputs.random_case(31, 300, 170, 12, 10, nT=5, n_crops=2)
-    r = ncc.ncc_correlate_direct(to_dev(w.image), to_dev(w.templates)).cpu().numpy()
+    r = ncc.ncc_correlate_direct(to_dev(w.image), to_dev(w.templates),
+                                 out=nan_map(5, w.Oy, w.Ox)).cpu().numpy()
     assert ncc.ncc_sync_status() == 0
     for t in range(5):
         ref = oracle.correlate(w.image, w.templates[t], threads=threads)
@@ -84,7 +80,7 @@ def test_direct_zero_variance_and_saturated(ncc):
     img = np.full((200, 300), 255, np.uint8)
     img[50:120, 60:200] = np.random.default_rng(5).integers(0, 256, (70, 140), dtype=np.uint8)
     T = img[60:76, 100:116].copy()
-    r = ncc.ncc_correlate_direct(to_dev(img), to_dev(T)).cpu().numpy()[0]
+    r = ncc.ncc_correlate_direct(to_dev(img), to_dev(T), out=nan_map(1, 185, 285)).cpu().numpy()[0]
     assert ncc.ncc_sync_status() == 0
     assert r[0, 0] == 0.0                              # a window of constant 255
     assert abs(r[60, 100] - 1.0) <= TOL

@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 import oracle
+from gpu_util import nan_map, to_dev
 from normalized_cross_correlation_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -17,17 +18,14 @@ pytestmark = pytest.mark.gpu
 TOL = 1e-5
 
 
-def to_dev(a):
-    import torch
-    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
-
-
 def separate(ncc, dimg, dt):
     S, Q = ncc.ncc_sat_build(dimg)
-    if dt.dim() == 3 and dt.shape[0] > 1:
-        out = ncc.ncc_correlate_bank(dimg, dt, S, Q)
+    nT, hT, wT = dt.shape
+    Oy, Ox = dimg.shape[0] - hT + 1, dimg.shape[1] - wT + 1
+    if nT > 1:
+        out = ncc.ncc_correlate_bank(dimg, dt, S, Q, out=nan_map(nT, Oy, Ox))
     else:
-        out = ncc.ncc_correlate(dimg, dt.reshape(dt.shape[-2:]), S, Q).unsqueeze(0)
+        out = ncc.ncc_correlate(dimg, dt[0], S, Q, out=nan_map(Oy, Ox)).unsqueeze(0)
     assert ncc.ncc_sync_status() == 0
     return S.cpu().numpy(), Q.cpu().numpy(), out.cpu().numpy()
 
@@ -48,7 +46,7 @@ def test_match_equals_separate_calls(ncc, W, H, wT, hT, nT):
     w = inputs.random_case(W * 7 + H * 3 + nT, W, H, wT, hT, nT=nT, n_crops=1)
     dimg, dt = to_dev(w.image), to_dev(w.templates)
     S0, Q0, r0 = separate(ncc, dimg, dt)
-    S, Q, r = ncc.ncc_match(dimg, dt)
+    S, Q, r = ncc.ncc_match(dimg, dt, out=nan_map(nT, w.Oy, w.Ox))
     assert ncc.ncc_sync_status() == 0
     np.testing.assert_array_equal(S.cpu().numpy(), S0)
     np.testing.assert_array_equal(Q.cpu().numpy(), Q0)
@@ -57,7 +55,7 @@ def test_match_equals_separate_calls(ncc, W, H, wT, hT, nT):
 
 def test_match_small_case_matches_oracle(ncc, threads):
     w = inputs.random_case(4242, 300, 200, 16, 16, nT=1, n_crops=1)
-    S, Q, r = ncc.ncc_match(to_dev(w.image), to_dev(w.templates))
+    S, Q, r = ncc.ncc_match(to_dev(w.image), to_dev(w.templates), out=nan_map(1, w.Oy, w.Ox))
     assert ncc.ncc_sync_status() == 0
     oS, oQ = oracle.sat(w.image)
     np.testing.assert_array_equal(S.cpu().numpy(), oS)

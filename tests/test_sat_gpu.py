@@ -115,3 +115,62 @@ def test_lookback_timeout_is_reported_and_recovers(ncc):
         np.testing.assert_array_equal(Q, oQ)
     other = rng.integers(0, 256, (300, 700), dtype=np.uint8)
     check_exact(ncc, other)
+
+
+def test_host_path_allocation_failure_reports_nomem_and_recovers(ncc):
+    """A device allocation that fails (forced by the host-side hook) makes
+    the call return NCC_ERR_NOMEM without launching anything; the next call
+    allocates and computes normally."""
+    w = inputs.random_case(404, 300, 200, 16, 16, nT=1, n_crops=1)
+    out = np.full((1, w.Oy, w.Ox), np.nan, np.float32)
+    ncc.ncc_debug_fail_alloc(1)
+    try:
+        with pytest.raises(ncc.NccError) as e:
+            ncc.ncc_match_host(w.image, w.templates, out)
+        assert e.value.code == ncc.NCC_ERR_NOMEM
+        assert np.all(np.isnan(out))                 # nothing ran
+    finally:
+        ncc.ncc_debug_fail_alloc(0)
+    assert ncc.ncc_sync_status() == 0
+    ncc.ncc_match_host(w.image, w.templates, out)
+    ref = oracle.correlate(w.image, w.templates[0])
+    np.testing.assert_allclose(out[0], ref, rtol=0, atol=1e-5)
+
+
+FRESH_PROCESS_NOMEM = r"""
+import sys
+import numpy as np
+import torch
+sys.path.insert(0, {root!r})
+import oracle
+from normalized_cross_correlation_gb300 import ncc
+img_np = np.random.default_rng(9).integers(0, 256, (300, 500), dtype=np.uint8)
+img = torch.from_numpy(img_np).cuda()
+ncc.ncc_debug_fail_alloc(1)            # the look-back workspace's first allocation fails
+try:
+    ncc.ncc_sat_build(img)
+    sys.exit(3)
+except ncc.NccError as e:
+    if e.code != ncc.NCC_ERR_NOMEM:
+        sys.exit(4)
+if ncc.ncc_sync_status() != 0:
+    sys.exit(5)
+S, Q = ncc.ncc_sat_build(img)          # allocates now
+if ncc.ncc_sync_status() != 0:
+    sys.exit(6)
+oS, oQ = oracle.sat(img_np)
+sys.exit(0 if np.array_equal(S.cpu().numpy(), oS) and np.array_equal(Q.cpu().numpy(), oQ) else 7)
+"""
+
+
+def test_workspace_allocation_failure_in_a_fresh_process(ncc):
+    """The SAT builder's look-back workspace is allocated on a device's first
+    build: in a fresh process, a forced failure there gives NCC_ERR_NOMEM,
+    and the following build allocates it and writes the oracle's tables."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = subprocess.run([sys.executable, "-c", FRESH_PROCESS_NOMEM.format(root=root)],
+                         capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, (res.returncode, res.stdout[-2000:], res.stderr[-2000:])

@@ -1,7 +1,8 @@
 """ncc_sat_build_noalloc: the table builder for callers that cannot allocate
-device memory (stream capture, host callbacks, real-time loops, frameworks
-that own every allocation).  It must give exactly the tables of the
-allocating entry point, call after call, from its fixed scratch array.
+device memory (host callbacks and real-time loops, where cudaMalloc may
+synchronize the device; frameworks that own every allocation).  It must give
+exactly the tables of the allocating entry point -- and so the oracle's --
+call after call, from its fixed scratch array.
 
 This file is collected last on purpose: it also has to pass after every
 other test has run in the same process (the scratch then holds an earlier
@@ -10,6 +11,7 @@ call sets up the scratch address)."""
 import numpy as np
 import pytest
 
+import oracle
 from normalized_cross_correlation_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -41,6 +43,9 @@ def test_noalloc_tables_equal_the_allocating_builder_twice_in_a_row(ncc):
         S, Q = call_noalloc(ncc, img)
         assert torch.equal(S, S_ref), "S differs from ncc_sat_build"
         assert torch.equal(Q, Q_ref), "Q differs from ncc_sat_build"
+        oS, oQ = oracle.sat(img_np)
+        np.testing.assert_array_equal(S.cpu().numpy(), oS)
+        np.testing.assert_array_equal(Q.cpu().numpy(), oQ)
     # and once more on the first image, after the scratch held the larger one
     img = torch.from_numpy(images[0]).cuda()
     S_ref, Q_ref = ncc.ncc_sat_build(img)
