@@ -1,11 +1,14 @@
 """Benchmark of the NCC hot path on GB300.
 
-One step = the whole path on one 4096x4096 uint8 image and one 16x16 uint8
-template: build both int64 summed-area tables, then the numerator and
-coefficients for all 4081 x 4081 valid shifts, in one ncc_match call (the
-correlation kernel overlaps the table build's tail).  The same steps are also
-timed as separate ncc_sat_build + ncc_correlate calls with an event between
-them, for the per-kernel times and rooflines.  Prints one JSON line: the
+One step = the whole path on a batch of 4096x4096 uint8 images with one 16x16
+uint8 template: for each image, build both int64 summed-area tables, then the
+numerator and coefficients for all 4081 x 4081 valid shifts, in one ncc_match
+call (the correlation kernel overlaps the table build's tail).  The batch is
+the workload image and seeded circular shifts of it, sized so a step lasts
+about 40 ms of device time (the clock sampler then sees the load).  The same
+steps are also timed as separate ncc_sat_build + ncc_correlate calls with
+events between the kernels, for the per-kernel times and rooflines, and the
+table build alone is timed on the 8192x8192 image.  Prints one JSON line: the
 throughput, per-kernel timings, the roofline of the dominant kernel, the CPU
 oracle baseline, the end-to-end figure and clocks.
 
@@ -68,6 +71,8 @@ N_SMS = 152
 # kernel changes, so a stale count is never reported.
 NCU_TRAFFIC_BYTES = {
     ("sat_build", "ncc_4096_t16"): 230.7e6,
+    ("sat_build", "large_8192_t64"): 1107.0e6,
+    ("sat_build", "sat_8192"): 1107.0e6,
     ("corr_dp4a", "ncc_4096_t16"): 337.7e6,
     ("bank_tc", "bank_2048_64x16"): 1075.6e6,
     ("corr_dp4a_direct", "ncc_4096_t16"): 26.3e6,
@@ -152,7 +157,8 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         loaded = [v for v in sm if v >= 0.5 * max(sm)] or sm
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "samples_under_load": len(loaded),
+                "reasons": sorted(reasons)}
 
 
 def oracle_sample_rate(w: inputs.Workload, band_rows: int, threads: int) -> tuple[float, float]:
@@ -204,6 +210,54 @@ def run_reference(args, w: inputs.Workload) -> dict:
     }
 
 
+def device_batch(torch, img, n: int):
+    """n distinct device images of img's shape and pixel distribution: img and
+    n-1 seeded circular shifts of it (see inputs.batch_shifts)."""
+    H, W = img.shape
+    shifts = inputs.batch_shifts(n, W, H)
+    return [img] + [torch.roll(img, shifts=(int(dy), int(dx)), dims=(0, 1))
+                    for dy, dx in shifts[1:]]
+
+
+def batch_size(per_call_ms: float, target_ms: float, image_bytes: int, cap_bytes: float) -> int:
+    """Images per step: enough that one step lasts about target_ms, bounded so
+    the batch's distinct images stay within cap_bytes of device memory."""
+    b = int(np.ceil(target_ms / max(per_call_ms, 1e-3)))
+    return int(max(1, min(b, cap_bytes // max(image_bytes, 1), 4096)))
+
+
+def timed_steps(torch, stream, flush, steps: int, body) -> list[float]:
+    """Times `steps` calls of body() with CUDA events on `stream`, the L2
+    flushed before each; returns milliseconds per step."""
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for k in range(steps):
+        flush.zero_()                          # L2 flushed between timed steps
+        ev0[k].record(stream)
+        body(k)
+        ev1[k].record(stream)
+    torch.cuda.synchronize()
+    return [ev0[k].elapsed_time(ev1[k]) for k in range(steps)]
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def run_gpu(args, w: inputs.Workload) -> dict | None:
     import torch
     from normalized_cross_correlation_gb300 import ncc
@@ -220,95 +274,135 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
     dev = torch.device("cuda", local)
 
     nT = w.nT
-    img = torch.from_numpy(w.image).to(dev)
+    img0 = torch.from_numpy(w.image).to(dev)
     S = torch.empty((w.H, w.W), dtype=torch.int64, device=dev)
     Q = torch.empty((w.H, w.W), dtype=torch.int64, device=dev)
     if nT:
         tmpl = torch.from_numpy(w.templates).to(dev)
         out = torch.empty((nT, w.Oy, w.Ox), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    ev_mid = None
 
     variant = SAT_VARIANTS[args.sat_variant]
+    # The whole path in one call: the table build, then the correlation,
+    # which (one template) overlaps the build's tail.  Only the single-pass
+    # builder lets its dependents start early; the compared builders run the
+    # two calls separately.
+    fused = bool(nT) and variant == 0
 
-    def step():
+    def sat(im, SS=S, QQ=Q):
         if variant == 0:
-            rc = L.ncc_sat_build(img.data_ptr(), w.W, w.H, S.data_ptr(), Q.data_ptr(), sh)
+            rc = L.ncc_sat_build(im.data_ptr(), im.shape[1], im.shape[0], SS.data_ptr(),
+                                 QQ.data_ptr(), sh)
         else:
-            rc = L.ncc_sat_build_variant(img.data_ptr(), w.W, w.H, S.data_ptr(), Q.data_ptr(),
-                                         variant, sh)
+            rc = L.ncc_sat_build_variant(im.data_ptr(), im.shape[1], im.shape[0], SS.data_ptr(),
+                                         QQ.data_ptr(), variant, sh)
         assert rc == 0, rc
-        if not nT:
-            return
-        ev_mid.record(stream)
+
+    def correlate(im):
         if nT == 1:
-            rc = L.ncc_correlate(img.data_ptr(), w.W, w.H, tmpl.data_ptr(), w.wT, w.hT,
+            rc = L.ncc_correlate(im.data_ptr(), w.W, w.H, tmpl.data_ptr(), w.wT, w.hT,
                                  S.data_ptr(), Q.data_ptr(), out.data_ptr(), sh)
         else:
-            rc = L.ncc_correlate_bank(img.data_ptr(), w.W, w.H, tmpl.data_ptr(), w.wT, w.hT, nT,
+            rc = L.ncc_correlate_bank(im.data_ptr(), w.W, w.H, tmpl.data_ptr(), w.wT, w.hT, nT,
                                       S.data_ptr(), Q.data_ptr(), out.data_ptr(), sh)
         assert rc == 0, rc
 
-    # The whole step in one call: the table build, then the correlation,
-    # which (one template) overlaps the build's tail.  Only the single-pass
-    # builder lets its dependents start early; the compared builders run
-    # the two calls above.
-    fused = bool(nT) and variant == 0
-
-    def step_fused():
-        rc = L.ncc_match(img.data_ptr(), w.W, w.H, tmpl.data_ptr(), w.wT, w.hT, nT,
+    def match(im):
+        rc = L.ncc_match(im.data_ptr(), w.W, w.H, tmpl.data_ptr(), w.wT, w.hT, nT,
                          S.data_ptr(), Q.data_ptr(), out.data_ptr(), sh)
         assert rc == 0, rc
 
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_m = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_f0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_f1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_mid = torch.cuda.Event(enable_timing=True)
+    def one_call(im):
+        if fused:
+            match(im)
+        else:
+            sat(im)
+            if nT:
+                correlate(im)
+
+    # warm-up, then a calibration of one call's time (untimed for the result)
     for _ in range(args.warmup):
         flush.zero_()
-        step()
-        if fused:
-            flush.zero_()
-            step_fused()
+        one_call(img0)
+    cal = timed_steps(torch, stream, flush, 3, lambda k: one_call(img0))
+    assert ncc.ncc_sync_status() == 0
+    B = args.batch or batch_size(statistics.mean(cal), args.step_ms, w.W * w.H, 4e9)
+    images = device_batch(torch, img0, B)
+    for im in images:                           # every image once, untimed
+        one_call(im)
     torch.cuda.synchronize()
     assert ncc.ncc_sync_status() == 0
+
+    # per-kernel events of the separate-call loop: SAT start, SAT end /
+    # correlation start, correlation end, for every image of every step
+    ev_s = [[torch.cuda.Event(enable_timing=True) for _ in range(B)] for _ in range(args.steps)]
+    ev_m = [[torch.cuda.Event(enable_timing=True) for _ in range(B)] for _ in range(args.steps)]
+    ev_e = [[torch.cuda.Event(enable_timing=True) for _ in range(B)] for _ in range(args.steps)]
+
+    def split_step(k):
+        for b, im in enumerate(images):
+            ev_s[k][b].record(stream)
+            sat(im)
+            ev_m[k][b].record(stream)
+            if nT:
+                correlate(im)
+            ev_e[k][b].record(stream)
+
+    def fused_step(k):
+        for im in images:
+            match(im)
+
+    # the table build alone on the 8192x8192 image of the large workload,
+    # where the 129 MB L2 cannot hold back any of the 1.07 GB of tables
+    # (prepared here, timed inside the sampled region below)
+    large = None
+    if args.sat_large and variant == 0 and w.W * w.H < 8192 * 8192:
+        bimg = torch.from_numpy(inputs.large_8192().image).to(dev)
+        S8 = torch.empty((8192, 8192), dtype=torch.int64, device=dev)
+        Q8 = torch.empty_like(S8)
+        for _ in range(3):
+            sat(bimg, S8, Q8)
+        cal8 = timed_steps(torch, stream, flush, 3, lambda k: sat(bimg, S8, Q8))
+        B8 = batch_size(statistics.mean(cal8), args.step_ms / 2, 8192 * 8192, 4e9)
+        large = (device_batch(torch, bimg, B8), S8, Q8)
+        del bimg
+        torch.cuda.synchronize()
+
+    def large_step(k):
+        bimgs, S8, Q8 = large
+        for im in bimgs:
+            sat(im, S8, Q8)
 
     clocks = ClockSampler(local)
     with clocks:
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
-        # timed region 1: the steps as a user runs them (ncc_match)
-        if fused:
-            for k in range(args.steps):
-                flush.zero_()                   # L2 flushed between timed steps
-                ev_f0[k].record(stream)
-                step_fused()
-                ev_f1[k].record(stream)
-        # timed region 2: the same steps as separate calls, with an event
+        # timed region 1: the steps as a user runs them (ncc_match per image)
+        t_fused = timed_steps(torch, stream, flush, args.steps, fused_step) if fused else None
+        # timed region 2: the same steps as separate calls, with events
         # between the kernels for the per-kernel times and rooflines
-        for k in range(args.steps):
-            flush.zero_()                       # L2 flushed between timed steps
-            ev_a[k].record(stream)
-            ev_mid = ev_m[k]
-            step()
-            if not nT:
-                ev_m[k].record(stream)
-            ev_b[k].record(stream)
-        torch.cuda.synchronize()
+        t_split = timed_steps(torch, stream, flush, args.steps, split_step)
+        # timed region 3: the table build alone at 8192x8192
+        t8 = timed_steps(torch, stream, flush, args.steps, large_step) if large else None
         if dist is not None:
             dist.barrier()
     assert ncc.ncc_sync_status() == 0
-    t_sat = [ev_a[k].elapsed_time(ev_m[k]) for k in range(args.steps)]
-    t_corr = [ev_m[k].elapsed_time(ev_b[k]) for k in range(args.steps)]
-    t_split = [a + b for a, b in zip(t_sat, t_corr)]
-    t_step = [ev_f0[k].elapsed_time(ev_f1[k]) for k in range(args.steps)] if fused else t_split
+    t_sat = [ev_s[k][b].elapsed_time(ev_m[k][b]) for k in range(args.steps) for b in range(B)]
+    t_corr = [ev_m[k][b].elapsed_time(ev_e[k][b]) for k in range(args.steps) for b in range(B)]
+    t_step = t_fused if fused else t_split
     ms_step = max_over_ranks(statistics.mean(t_step), dist, dev)
     ms_split = max_over_ranks(statistics.mean(t_split), dist, dev)
-    coeffs = nT * w.Ox * w.Oy if nT else w.W * w.H
-    value = job_rate(coeffs, ws, ms_step)
+    per_image = nT * w.Ox * w.Oy if nT else w.W * w.H
+    value = job_rate(B * per_image, ws, ms_step)
+    del images
+    sat_large = None
+    if large:
+        B8 = len(large[0])
+        sat_large = {"image": "8192x8192 u8 (large_8192_t64) and seeded circular shifts",
+                     "images_per_step": B8,
+                     "ms": max_over_ranks(statistics.mean(t8) / B8, dist, dev)}
+        large = None
 
     # end to end through the host-buffer entry point (pinned host memory)
     e2e = None
@@ -326,9 +420,9 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
             ncc.ncc_match_host(himg, htmp, hout)      # synchronizes the stream
             e2e_t.append(time.perf_counter() - t0)
         e2e_ms = max_over_ranks(statistics.mean(e2e_t) * 1e3, dist, dev)
-        e2e = {"value": job_rate(coeffs, ws, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
+        e2e = {"value": job_rate(per_image, ws, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": int(w.image.nbytes + w.templates.nbytes),
-               "d2h_bytes_per_step": int(coeffs * 4)}
+               "d2h_bytes_per_step": int(per_image * 4)}
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -339,35 +433,42 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
     hbm = float(peaks["hbm_gbs"])
     sat_ms, corr_ms = statistics.mean(t_sat), statistics.mean(t_corr)
     sat_gbs = SAT_BYTES_PER_PX * w.W * w.H / (sat_ms * 1e-3) / 1e9
-    roof_sat = {"kernel": "sat_build", "bound": "hbm", "achieved": sat_gbs, "peak": hbm,
-                "unit": "GB/s", "frac": sat_gbs / hbm,
+    roof_sat = {"kernel": "sat_build", "workload": w.name, "bound": "hbm", "achieved": sat_gbs,
+                "peak": hbm, "unit": "GB/s", "frac": sat_gbs / hbm,
                 "traffic": NCU_TRAFFIC_BYTES.get(("sat_build", w.name)) if variant == 0 else None,
                 "peak_source": peaks["source"]}
     rooflines = [roof_sat]
+    if sat_large:
+        gbs8 = SAT_BYTES_PER_PX * 8192 * 8192 / (sat_large["ms"] * 1e-3) / 1e9
+        sat_large.update({"GB/s": gbs8, "frac_of_hbm": gbs8 / hbm})
+        rooflines.append({"kernel": "sat_build", "workload": "large_8192_t64", "bound": "hbm",
+                          "achieved": gbs8, "peak": hbm, "unit": "GB/s", "frac": gbs8 / hbm,
+                          "traffic": NCU_TRAFFIC_BYTES.get(("sat_build", "large_8192_t64")),
+                          "peak_source": peaks["source"]})
     corr = None
     dominant = roof_sat
     if nT:
-        macs = coeffs * w.wT * w.hT
+        macs = per_image * w.wT * w.hT
         if nT == 1:
             # S and Q corners (16 B after reuse) + 1 B image + 4 B out per coefficient
-            corr_bytes = 21 * w.Ox * w.Oy
+            corr_bytes = CORR_BYTES_PER_COEFF * w.Ox * w.Oy
             dp4a = w.Ox * w.Oy * ((w.wT + 3) // 4) * w.hT
             alu_peak = DP4A_PER_SM_CLK * N_SMS * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
-            r2 = {"kernel": "corr_dp4a", "bound": "alu",
+            r2 = {"kernel": "corr_dp4a", "workload": w.name, "bound": "alu",
                   "achieved": dp4a / (corr_ms * 1e-3) / 1e12, "peak": alu_peak / 1e12,
                   "unit": "Tdp4a/s", "frac": dp4a / (corr_ms * 1e-3) / alu_peak,
                   "traffic": NCU_TRAFFIC_BYTES.get(("corr_dp4a", w.name))}
         else:
             # 4 B out per coefficient + S and Q (16 B) + image (1 B) per shift
-            corr_bytes = 4 * coeffs + 17 * w.Ox * w.Oy
+            corr_bytes = 4 * per_image + 17 * w.Ox * w.Oy
             tflops = 2.0 * macs / (corr_ms * 1e-3) / 1e12
             peak_tc = float(peaks.get("bf16_tflops", 1900.0))  # f16 runs at the bf16 rate
-            r2 = {"kernel": "bank_tc", "bound": "tensor", "achieved": tflops, "peak": peak_tc,
-                  "unit": "TFLOP/s", "frac": tflops / peak_tc,
+            r2 = {"kernel": "bank_tc", "workload": w.name, "bound": "tensor", "achieved": tflops,
+                  "peak": peak_tc, "unit": "TFLOP/s", "frac": tflops / peak_tc,
                   "traffic": NCU_TRAFFIC_BYTES.get(("bank_tc", w.name))}
         corr_gbs = corr_bytes / (corr_ms * 1e-3) / 1e9
-        r1 = {"kernel": r2["kernel"], "bound": "hbm", "achieved": corr_gbs, "peak": hbm,
-              "unit": "GB/s", "frac": corr_gbs / hbm, "traffic": r2["traffic"]}
+        r1 = {"kernel": r2["kernel"], "workload": w.name, "bound": "hbm", "achieved": corr_gbs,
+              "peak": hbm, "unit": "GB/s", "frac": corr_gbs / hbm, "traffic": r2["traffic"]}
         rooflines += [r1, r2]
         corr_roof = max(r1, r2, key=lambda r: r["frac"])
         dominant = roof_sat if sat_ms >= corr_ms else corr_roof
@@ -380,12 +481,20 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
         threads = oracle.default_threads()
         rows = sample_rows(w, args.ref_rows)
         rate, dt = oracle_sample_rate(w, rows, threads)
-        cpu = {"value": rate, "unit": UNIT, "cores": threads,
-               "kind": "oracle",
+        rows1 = max(1, rows // 4)
+        rate1, dt1 = oracle_sample_rate(w, rows1, 1)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "model": cpu_model(),
                "sample": f"tables of the top {rows + w.hT - 1} image rows + all "
-                         f"{nT}x{rows}x{w.Ox} coefficients of those rows ({dt:.1f} s)"}
+                         f"{nT}x{rows}x{w.Ox} coefficients of those rows ({dt:.1f} s)",
+               "single_thread": {"value": rate1, "unit": UNIT, "cores": 1,
+                                 "sample": f"the same for the top {rows1} output rows "
+                                           f"({dt1:.1f} s)"}}
 
     metric = METRIC if w.name == DEFAULT_WORKLOAD else f"NCC coefficients/s ({w.name})"
+    calls = ("ncc_sat_build + " + ("ncc_correlate" if nT == 1 else
+                                   "ncc_correlate_bank" if nT else "nothing"))
+    launches_per_image = (1 if nT else 0) + (1 if variant == 0 else 2)
     return {
         "metric": metric, "value": value, "unit": UNIT if nT else "pixels/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -393,24 +502,27 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
         "data": "synthetic",
         "config": {"workload": w.name, "image": f"{w.W}x{w.H} u8",
                    "templates": f"{nT}x{w.hT}x{w.wT} u8" if nT else None,
-                   "step": ("ncc_match (ncc_sat_build, then ncc_correlate" +
+                   "images_per_step": B,
+                   "batch": "the workload image and seeded circular shifts of it, one call each",
+                   "step": ("ncc_match per image (ncc_sat_build, then ncc_correlate" +
                             (", overlapped)" if nT == 1 else "_bank)")) if fused else
-                           "ncc_sat_build + " + ("ncc_correlate" if nT == 1 else
-                                                 "ncc_correlate_bank" if nT else "nothing"),
+                           calls + " per image",
                    "sat_builder": args.sat_variant,
-                   "l2": "flushed between timed steps (512 MB write)"},
-        "split_step": {"ms": ms_split, "calls": "ncc_sat_build + " +
-                       ("ncc_correlate" if nT == 1 else "ncc_correlate_bank" if nT else "nothing"),
+                   "l2": "flushed between timed steps (512 MB write); within a step the images "
+                         "differ and each one's tables exceed L2"},
+        "ms_per_image": ms_step / B,
+        "split_step": {"ms": ms_split, "ms_per_image": ms_split / B, "calls": calls,
                        "note": "the per-kernel times and rooflines come from these steps"},
         "sat_build": {"ms": sat_ms, "GB/s": sat_gbs, "frac_of_hbm": sat_gbs / hbm},
+        "sat_build_8192": sat_large,
         "correlate": corr,
         "roofline": {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")},
         "rooflines": rooflines,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        # this library's kernels in both timed loops (the same kernels per step)
-        "gpu_launches": ((1 if nT else 0) + (1 if variant == 0 else 2)) * args.steps *
-                        (2 if fused else 1),
+        # this library's kernels in the timed loops
+        "gpu_launches": launches_per_image * B * args.steps * (2 if fused else 1) +
+                        (sat_large["images_per_step"] * args.steps if sat_large else 0),
         "clocks": clocks.summary(),
     }
 
@@ -433,41 +545,39 @@ def run_gpu_direct(args, w: inputs.Workload) -> dict | None:
     sh = stream.cuda_stream
     dev = torch.device("cuda", local)
     nT = w.nT
-    img = torch.from_numpy(w.image).to(dev)
+    img0 = torch.from_numpy(w.image).to(dev)
     tmpl = torch.from_numpy(w.templates).to(dev)
     out = torch.empty((nT, w.Oy, w.Ox), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def step():
-        rc = L.ncc_correlate_direct(img.data_ptr(), w.W, w.H, tmpl.data_ptr(), w.wT, w.hT, nT,
+    def call(im):
+        rc = L.ncc_correlate_direct(im.data_ptr(), w.W, w.H, tmpl.data_ptr(), w.wT, w.hT, nT,
                                     out.data_ptr(), sh)
         assert rc == 0, rc
 
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     for _ in range(args.warmup):
         flush.zero_()
-        step()
-    torch.cuda.synchronize()
+        call(img0)
+    cal = timed_steps(torch, stream, flush, 3, lambda k: call(img0))
     assert ncc.ncc_sync_status() == 0
+    B = args.batch or batch_size(statistics.mean(cal), args.step_ms, w.W * w.H, 4e9)
+    images = device_batch(torch, img0, B)
+    for im in images:
+        call(im)
+    torch.cuda.synchronize()
     clocks = ClockSampler(local)
     with clocks:
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
-        for k in range(args.steps):
-            flush.zero_()                       # L2 flushed between timed steps
-            ev_a[k].record(stream)
-            step()
-            ev_b[k].record(stream)
-        torch.cuda.synchronize()
+        t = timed_steps(torch, stream, flush, args.steps, lambda k: [call(im) for im in images])
         if dist is not None:
             dist.barrier()
     assert ncc.ncc_sync_status() == 0
-    t = [ev_a[k].elapsed_time(ev_b[k]) for k in range(args.steps)]
-    ms = max_over_ranks(statistics.mean(t), dist, dev)
+    ms_step = max_over_ranks(statistics.mean(t), dist, dev)
+    ms = ms_step / B                            # one image
     coeffs = nT * w.Ox * w.Oy
-    value = job_rate(coeffs, ws, ms)
+    value = job_rate(B * coeffs, ws, ms_step)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -487,11 +597,14 @@ def run_gpu_direct(args, w: inputs.Workload) -> dict | None:
     dominant = max(r_alu, r_hbm, key=lambda r: r["frac"])
     return {
         "metric": f"NCC coefficients/s ({w.name}, direct moments)", "value": value, "unit": UNIT,
-        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "ms_per_image": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
         "data": "synthetic",
         "config": {"workload": w.name, "image": f"{w.W}x{w.H} u8",
-                   "templates": f"{nT}x{w.hT}x{w.wT} u8", "step": "ncc_correlate_direct",
+                   "templates": f"{nT}x{w.hT}x{w.wT} u8", "images_per_step": B,
+                   "batch": "the workload image and seeded circular shifts of it, one call each",
+                   "step": "ncc_correlate_direct per image",
                    "moments": "direct (staged image tile, no summed-area tables)",
                    "l2": "flushed between timed steps (512 MB write)"},
         "correlate": {"kernel": "corr_dp4a_direct", "ms": ms, "GB/s": gbs,
@@ -500,7 +613,7 @@ def run_gpu_direct(args, w: inputs.Workload) -> dict | None:
         "rooflines": [r_alu, r_hbm],
         "cpu_baseline": None,
         "e2e": None,
-        "gpu_launches": nT * args.steps,
+        "gpu_launches": nT * B * args.steps,
         "clocks": clocks.summary(),
     }
 
@@ -515,6 +628,12 @@ def main():
                     help="output rows of the oracle's bounded sample per step "
                          "(default: about 2e10 multiply-adds' worth)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="images per timed step (default: enough for about --step-ms)")
+    ap.add_argument("--step-ms", type=float, default=40.0,
+                    help="target device time of one timed step, which sets the batch")
+    ap.add_argument("--no-sat-large", dest="sat_large", action="store_false",
+                    help="skip the table-build roofline on the 8192x8192 image")
     ap.add_argument("--sat-variant", default="fused", choices=sorted(SAT_VARIANTS),
                     help="summed-area-table builder: the single pass (default) or one of the "
                          "builds it is compared with")

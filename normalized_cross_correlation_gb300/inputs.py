@@ -141,6 +141,11 @@ def large_8192(seed: int = 4) -> Workload:
     return Workload("large_8192_t64", img, T, [(0, 4000, 6000)])
 
 
+def sat_8192(seed: int = 4) -> Workload:
+    """The 8192x8192 image of :func:`large_8192`, tables only (no template)."""
+    return Workload("sat_8192", large_8192(seed).image, None, [])
+
+
 NAMED = {
     "tiny_ncc_256_t16": tiny_ncc,
     "smooth_1024_t32": smooth_1024,
@@ -148,7 +153,18 @@ NAMED = {
     "ncc_4096_t16": headline_4096,
     "bank_2048_64x16": bank_2048,
     "large_8192_t64": large_8192,
+    "sat_8192": sat_8192,
 }
+
+
+def batch_shifts(n: int, W: int, H: int, seed: int = 77) -> np.ndarray:
+    """Seeded circular shifts (dy, dx) that turn one workload image into a
+    batch of n distinct images of the same pixel distribution (image 0 is
+    unshifted).  Only offsets are drawn here; applying them is a copy."""
+    rng = np.random.default_rng(seed)
+    d = np.stack([rng.integers(1, max(2, H), n), rng.integers(1, max(2, W), n)], axis=1)
+    d[0] = 0
+    return d
 
 
 def random_case(seed: int, W: int, H: int, wT: int, hT: int, nT: int = 1,
