@@ -76,6 +76,7 @@ NCU_TRAFFIC_BYTES = {
     ("corr_dp4a", "ncc_4096_t16"): 337.7e6,
     ("bank_tc", "bank_2048_64x16"): 1075.6e6,
     ("corr_dp4a_direct", "ncc_4096_t16"): 26.3e6,
+    ("corr_toeplitz_tc", "large_8192_t64"): 1476.9e6,
 }
 
 
@@ -326,6 +327,7 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
         one_call(img0)
     cal = timed_steps(torch, stream, flush, 3, lambda k: one_call(img0))
     assert ncc.ncc_sync_status() == 0
+    path = ncc.ncc_debug_last_path() if nT else ncc.NCC_PATH_NONE   # the kernel that ran
     B = args.batch or batch_size(statistics.mean(cal), args.step_ms, w.W * w.H, 4e9)
     images = device_batch(torch, img0, B)
     for im in images:                           # every image once, untimed
@@ -449,7 +451,16 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
     dominant = roof_sat
     if nT:
         macs = per_image * w.wT * w.hT
-        if nT == 1:
+        if nT == 1 and path == ncc.NCC_PATH_TOEPLITZ:
+            # useful multiply-adds only (the Toeplitz form issues about Kp/wT
+            # times as many) against the f16 tensor rate (= the bf16 rate)
+            corr_bytes = CORR_BYTES_PER_COEFF * w.Ox * w.Oy
+            tflops = 2.0 * macs / (corr_ms * 1e-3) / 1e12
+            peak_tc = float(peaks.get("bf16_tflops", 1900.0))
+            r2 = {"kernel": "corr_toeplitz_tc", "workload": w.name, "bound": "tensor",
+                  "achieved": tflops, "peak": peak_tc, "unit": "TFLOP/s", "frac": tflops / peak_tc,
+                  "traffic": NCU_TRAFFIC_BYTES.get(("corr_toeplitz_tc", w.name))}
+        elif nT == 1:
             # S and Q corners (16 B after reuse) + 1 B image + 4 B out per coefficient
             corr_bytes = CORR_BYTES_PER_COEFF * w.Ox * w.Oy
             dp4a = w.Ox * w.Oy * ((w.wT + 3) // 4) * w.hT

@@ -42,15 +42,19 @@ enum ncc_path_code {
     NCC_PATH_NONE = 0,
     NCC_PATH_DP4A = 1,     /* single template, integer dot products         */
     NCC_PATH_TENSOR = 2,   /* single template, tcgen05 tensor cores          */
-    NCC_PATH_BANK = 3      /* template bank, tcgen05 tensor cores            */
+    NCC_PATH_BANK = 3,     /* template bank, tcgen05 tensor cores            */
+    NCC_PATH_TOEPLITZ = 4  /* single large template, tcgen05 Toeplitz product */
 };
 
 /*
  * ncc_debug_set_path -- selects the single-template kernel that
  * ncc_correlate, ncc_correlate_moments and ncc_correlate_bank (for banks the
- * bank kernel does not take) use.  0 = automatic (dp4a), NCC_PATH_DP4A =
- * dp4a, NCC_PATH_TENSOR = tensor cores (NCC_ERR_UNSUPPORTED where they do not
- * apply).  Process-wide; not for concurrent use.
+ * bank kernel does not take) use.  0 = automatic (the Toeplitz tensor-core
+ * kernel for templates at least 48 pixels wide where it applies, else
+ * dp4a), NCC_PATH_DP4A = dp4a, NCC_PATH_TENSOR = the row-window tensor-core
+ * kernel, NCC_PATH_TOEPLITZ = the Toeplitz tensor-core kernel
+ * (NCC_ERR_UNSUPPORTED where the forced kernel does not apply).
+ * Process-wide; not for concurrent use.
  * Returns NCC_OK, or NCC_ERR_INVALID_ARG for another value.
  */
 int ncc_debug_set_path(int path);

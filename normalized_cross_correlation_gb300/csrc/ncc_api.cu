@@ -38,6 +38,8 @@ void set_last_path(int path) {
 }
 
 constexpr int kMaxW = 66051;  // 66051 * 255^2 < 2^32: a row's running sum of squares fits uint32
+// Narrowest template that automatic selection gives the Toeplitz kernel.
+constexpr int kToeplitzMinWidth = 48;
 constexpr long long kMaxN = 66051;  // wT*hT*255^2 < 2^32: SumIT fits uint32
 
 int status_ptr(int **out) {
@@ -149,7 +151,13 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
         return rc;
     }
     if (direct) path = NCC_PATH_DP4A;  // the direct moments exist on the dp4a kernel only
-    if (path != NCC_PATH_TENSOR && !ncc::corr_dp4a_supported(wT, hT)) return NCC_ERR_UNSUPPORTED;
+    // Automatic selection: the Toeplitz tensor-core product for wide
+    // templates, whose numerator dominates; dp4a otherwise.
+    const bool toeplitz = ncc::corr_toeplitz_supported(wT, hT) &&
+                          (path == NCC_PATH_TOEPLITZ || (path == 0 && wT >= kToeplitzMinWidth));
+    if (path == NCC_PATH_TOEPLITZ && !toeplitz) return NCC_ERR_UNSUPPORTED;
+    if (path != NCC_PATH_TENSOR && !toeplitz && !ncc::corr_dp4a_supported(wT, hT))
+        return NCC_ERR_UNSUPPORTED;
     int used = NCC_PATH_NONE;
     for (int t = 0; t < nT; ++t) {
         ncc::CorrArgs a;
@@ -174,8 +182,16 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
             e = ncc::corr_tc_launch(a, stream);
             if (e == cudaSuccess) used = NCC_PATH_TENSOR;
         }
+        if (e == cudaErrorNotSupported && toeplitz) {
+            // plain stream order: behind the table build the early start
+            // measured slower for this kernel (8192x8192, 64x64: 2.19 ms per
+            // image against 1.87 ms as two calls), its CTAs taking whole SMs
+            a.overlap_prev = false;
+            e = ncc::corr_toeplitz_launch(a, stream);
+            if (e == cudaSuccess) used = NCC_PATH_TOEPLITZ;
+        }
         if (e == cudaErrorNotSupported) {
-            if (path == NCC_PATH_TENSOR) return NCC_ERR_UNSUPPORTED;
+            if (path == NCC_PATH_TENSOR || path == NCC_PATH_TOEPLITZ) return NCC_ERR_UNSUPPORTED;
             e = ncc::corr_dp4a_launch(a, stream);
             if (e == cudaSuccess) used = NCC_PATH_DP4A;
         }
@@ -423,7 +439,8 @@ const char *ncc_status_string(int status) {
 int ncc_version(void) { return (0 << 16) | 1; }
 
 int ncc_debug_set_path(int path) {
-    if (path != 0 && path != NCC_PATH_DP4A && path != NCC_PATH_TENSOR) return NCC_ERR_INVALID_ARG;
+    if (path != 0 && path != NCC_PATH_DP4A && path != NCC_PATH_TENSOR && path != NCC_PATH_TOEPLITZ)
+        return NCC_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(g_mutex);
     g_path = path;
     return NCC_OK;

@@ -178,6 +178,12 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream);
 // cudaErrorNotSupported, launching nothing, when the shape does not fit.
 bool corr_tc_supported(const CorrArgs &a);
 cudaError_t corr_tc_launch(const CorrArgs &a, cudaStream_t stream);
+// The same as a Toeplitz matrix product on the tensor cores (tcgen05, exact
+// centered f16 operands, fp32 accumulation in groups of at most 1024
+// products): wT <= 65 and a tile that fits two CTAs per SM.  Honours
+// CorrArgs::overlap_prev; no direct moments.
+bool corr_toeplitz_supported(int wT, int hT);
+cudaError_t corr_toeplitz_launch(const CorrArgs &a, cudaStream_t stream);
 
 // Template-bank correlation on the tensor cores (tcgen05, f16 operands,
 // fp32 accumulation; exact while wT*hT*255^2 < 2^24).
