@@ -26,7 +26,7 @@
 //   warp 0     allocates tensor memory; one thread issues the MMAs and the
 //              commits (tcgen05.commit -> mbarrier),
 //   warps 1-3  convert image rows (u8 -> f16 shifted copies) into a ring of
-//              A buffers in shared memory,
+//              A buffers in shared memory, each warp every third row,
 //   warps 4-11 epilogue: two warps per tensor-memory lane quarter (one per
 //              half of the template columns); tcgen05.ld of the accumulator
 //              row of its shift, box sums from S and Q once per shift
@@ -108,16 +108,21 @@ bool make_geom(int wT, int hT, int nT, bool pair, BankGeom &g) {
     if (g.tmemCols > kMaxTmemCols) return false;
     g.xBlocks = 15 + 2 * g.nK16;
     g.xBytes = g.xBlocks * 128;
-    g.nx = hT + 4;
     g.bBytes = pair ? g.nK16 * 2 * (hT + 2) * g.nTpad * 16 : hT * g.nK16 * g.nTpad * 32;
     g.offB = 0;
     g.offX = (g.bBytes + 1023) / 1024 * 1024;
-    g.offSt = g.offX + g.nx * g.xBytes;
-    const int stBytes = g.nTpad * 8;   // float2 {SumT, 1/sqrt(vT)} per template
-    g.offBar = (g.offSt + stBytes + 15) / 16 * 16;
-    const int barBytes = (2 * g.nx + 2 * g.na) * 8 + 16;
-    g.smemBytes = g.offBar + barBytes + 1024;  // + alignment slack
-    return g.smemBytes <= kMaxSmem;
+    // The ring of converted image rows: an accumulator uses hT+1 of them at
+    // once, so the converters run ahead by nx - hT - 1 rows.  As many spare
+    // rows as fit (up to 16), at least 3.
+    for (g.nx = hT + 16; g.nx >= hT + 4; --g.nx) {
+        g.offSt = g.offX + g.nx * g.xBytes;
+        const int stBytes = g.nTpad * 8;   // float2 {SumT, 1/sqrt(vT)} per template
+        g.offBar = (g.offSt + stBytes + 15) / 16 * 16;
+        const int barBytes = (2 * g.nx + 2 * g.na) * 8 + 16;
+        g.smemBytes = g.offBar + barBytes + 1024;  // + alignment slack
+        if (g.smemBytes <= kMaxSmem) return true;
+    }
+    return false;
 }
 
 struct BParams {
@@ -206,22 +211,33 @@ __device__ __forceinline__ void mbar_wait_warp(unsigned long long *b, uint32_t p
     if (!__shfl_sync(0xffffffffu, done, 0)) mbar_wait(b, parity, abort, status);
 }
 
-// Issue helpers for a warp that runs the MMA loop uniformly: only the lane
-// with `leader` set issues (a predicate, not a branch, so the descriptor
-// arithmetic stays warp-uniform).
-__device__ __forceinline__ void tc_commit_if(unsigned long long *b, bool leader) {
-    asm volatile("{ .reg .pred q; setp.ne.b32 q, %1, 0;\n"
-                 "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }"
-                 ::"r"(saddr(b)), "r"((uint32_t)leader) : "memory");
+// Non-blocking test of a phase: its result can be consumed later, so the
+// test's latency overlaps whatever the thread issues meanwhile.
+__device__ __forceinline__ uint32_t mbar_test(unsigned long long *b, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred P; mbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2; selp.u32 %0, 1, 0, P; }"
+        : "=r"(done) : "r"(saddr(b)), "r"(parity) : "memory");
+    return done;
 }
 
-__device__ __forceinline__ void tc_mma_if(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t acc, bool leader) {
-    asm volatile("{ .reg .pred p, q; setp.ne.b32 p, %4, 0; setp.ne.b32 q, %5, 0;\n"
-                 "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
-                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"((uint32_t)leader) : "memory");
+// Bounded wait by one thread (mbar_wait's loop without the warp exchange).
+__device__ __forceinline__ void mbar_wait_lane(unsigned long long *b, uint32_t parity, int *abort,
+                                               int *status) {
+    mbar_wait(b, parity, abort, status);
 }
 
+__device__ __forceinline__ void tc_commit(unsigned long long *b) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(saddr(b)) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
 
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile(
@@ -295,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                                  (n < p.nT && v2 > 0) ? __frsqrt_rn(u64_to_f32((unsigned long long)v2)) : 0.f);
         }
         if (tid == 0) {
-            for (int i = 0; i < g.nx; ++i) { mbar_init(&xfull[i], kProducers / 32); mbar_init(&xempty[i], 1); }
+            for (int i = 0; i < g.nx; ++i) { mbar_init(&xfull[i], 1); mbar_init(&xempty[i], 1); }
             for (int i = 0; i < g.na; ++i) { mbar_init(&afull[i], 1); mbar_init(&aempty[i], kEpiThreads / 32); }
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             s_abort = 0;
@@ -325,121 +341,177 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
         const int nrows = ty + p.hT - 1;
 
         if (warp >= 1 && warp <= 3) {
-            // ---- producers: image rows -> f16 shifted-copy A buffers ----
-            const int pt = tid - 32;
+            // ---- producers: image rows -> f16 shifted-copy A buffers.  Each of
+            // the three warps converts every third row on its own, with all of
+            // a row's loads issued before its conversions, so that three rows
+            // are in flight at once (a row done by all three warps together
+            // was latency-bound, one global load round trip per row) ----
+            const int cw = warp - 1;
             const bool aligned8 = (p.W % 8 == 0) && ((uintptr_t)p.img % 8 == 0);
-            for (int rl = 0; rl < nrows; ++rl) {
+            constexpr int kMaxChunks = 8;  // chunk rows per lane: (15 + 2*nK16)*8 / 32
+            const int nChunkRows = g.xBlocks * 8;
+            for (int rl = cw; rl < nrows; rl += kProducers / 32) {
                 const uint32_t q = rowSeq + rl, slot = q % g.nx, k = q / g.nx;
                 if (k > 0) mbar_wait_warp(&xempty[slot], (k - 1) & 1, &s_abort, p.status);
                 uint8_t *X = smem + g.offX + slot * g.xBytes;
                 const uint8_t *src = p.img + (size_t)(y0 + rl) * p.W;
-                for (int row = pt; row < g.xBlocks * 8; row += kProducers) {
-                    const int xb = x0 + 8 * (row >> 3), sh = row & 7;
-                    const int c0 = xb + sh;  // pixel of element 0
-                    uint32_t w0 = 0, w1 = 0;
-                    if (aligned8 && xb + 16 <= p.W) {
-                        // two aligned 8-byte loads, then a funnel shift by sh bytes
-                        const uint2 lo = __ldg(reinterpret_cast<const uint2 *>(src + xb));
-                        const uint2 hi = __ldg(reinterpret_cast<const uint2 *>(src + xb + 8));
-                        const bool up = sh >= 4;
-                        const uint32_t a0 = up ? lo.y : lo.x, a1 = up ? hi.x : lo.y,
-                                       a2 = up ? hi.y : hi.x;
-                        w0 = __funnelshift_r(a0, a1, 8u * (uint32_t)(sh & 3));
-                        w1 = __funnelshift_r(a1, a2, 8u * (uint32_t)(sh & 3));
-                    } else {
+                for (int r0 = 0; r0 < nChunkRows; r0 += 32 * kMaxChunks) {
+                    uint2 lo[kMaxChunks], hi[kMaxChunks];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            if (c0 + e < p.W) w0 |= (uint32_t)__ldg(src + c0 + e) << (8 * e);
-                            if (c0 + 4 + e < p.W) w1 |= (uint32_t)__ldg(src + c0 + 4 + e) << (8 * e);
+                    for (int i = 0; i < kMaxChunks; ++i) {
+                        const int row = r0 + lane + 32 * i;
+                        const int xb = x0 + 8 * (row >> 3);
+                        lo[i] = hi[i] = make_uint2(0, 0);
+                        if (row < nChunkRows && aligned8 && xb + 16 <= p.W) {
+                            lo[i] = __ldg(reinterpret_cast<const uint2 *>(src + xb));
+                            hi[i] = __ldg(reinterpret_cast<const uint2 *>(src + xb + 8));
                         }
                     }
-                    uint4 h;
-                    h.x = bytes_to_h2(w0, 0x4140);
-                    h.y = bytes_to_h2(w0, 0x4342);
-                    h.z = bytes_to_h2(w1, 0x4140);
-                    h.w = bytes_to_h2(w1, 0x4342);
-                    *reinterpret_cast<uint4 *>(X + row * 16) = h;
+#pragma unroll
+                    for (int i = 0; i < kMaxChunks; ++i) {
+                        const int row = r0 + lane + 32 * i;
+                        if (row >= nChunkRows) break;
+                        const int xb = x0 + 8 * (row >> 3), sh = row & 7;
+                        const int c0 = xb + sh;  // pixel of element 0
+                        uint32_t w0 = 0, w1 = 0;
+                        if (aligned8 && xb + 16 <= p.W) {
+                            // a funnel shift by sh bytes of the two aligned 8-byte loads
+                            const bool up = sh >= 4;
+                            const uint32_t a0 = up ? lo[i].y : lo[i].x, a1 = up ? hi[i].x : lo[i].y,
+                                           a2 = up ? hi[i].y : hi[i].x;
+                            w0 = __funnelshift_r(a0, a1, 8u * (uint32_t)(sh & 3));
+                            w1 = __funnelshift_r(a1, a2, 8u * (uint32_t)(sh & 3));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if (c0 + e < p.W) w0 |= (uint32_t)__ldg(src + c0 + e) << (8 * e);
+                                if (c0 + 4 + e < p.W) w1 |= (uint32_t)__ldg(src + c0 + 4 + e) << (8 * e);
+                            }
+                        }
+                        uint4 h;
+                        h.x = bytes_to_h2(w0, 0x4140);
+                        h.y = bytes_to_h2(w0, 0x4342);
+                        h.z = bytes_to_h2(w1, 0x4140);
+                        h.w = bytes_to_h2(w1, 0x4342);
+                        *reinterpret_cast<uint4 *>(X + row * 16) = h;
+                    }
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&xfull[slot]);
             }
         } else if (warp == 0) {
-            // ---- MMA issuer ----
-            // Descriptors are linear in the shared address (field = addr >> 4),
-            // so the loop only adds precomputed steps: no divisions per MMA.
-            // The whole warp runs the loop (warp-uniform descriptors); lane 0
-            // alone issues the MMAs and commits.
-            {
-                const bool leader = lane == 0;
+            // ---- MMA issuer: lane 0 alone.  The tensor pipe accepts an MMA
+            // only about one instruction ahead of the one it executes, so a
+            // wait between MMAs leaves it idle (a test of even a completed
+            // mbarrier takes some 200 cycles).  Before it issues an
+            // accumulator's MMAs, the issuer therefore tests (without
+            // blocking) the barriers of the next accumulator -- its
+            // accumulator stage and the image rows it needs -- and after them
+            // waits only for what the tests did not find complete.
+            // Descriptors are linear in the shared address (field = addr >> 4)
+            // and slots and phases advance incrementally: no divisions. ----
+            if (lane == 0) {
                 const uint64_t adesc0 = smem_desc(saddr(smem + g.offX), 128, 128);
                 const uint64_t bdesc0 = smem_desc(saddr(smem + g.offB), g.nTpad * 16, 128);
                 const uint32_t xStep = (uint32_t)g.xBytes >> 4;                 // next A buffer
                 const uint32_t bRow = (uint32_t)(g.nK16 * g.nTpad * 32) >> 4;  // next template row
                 const uint32_t bChunk = (uint32_t)(g.nTpad * 32) >> 4;         // next K chunk
-                const uint32_t slot0 = rowSeq % g.nx;                           // slot of image row y0
-                uint32_t readySlot = slot0;
-                int ready = 0;  // image rows of this tile known to be converted
-                if (kPair) {
-                    // B window of image row d: blocks hT-d and hT-d+1 (see make_geom)
-                    const uint64_t bdescP = smem_desc(saddr(smem + g.offB), (uint32_t)((p.hT + 2) * g.nTpad * 16), 128);
-                    const uint32_t bBlk = (uint32_t)(g.nTpad * 16) >> 4;
-                    const uint32_t bChunkP = (uint32_t)(2 * (p.hT + 2) * g.nTpad * 16) >> 4;
-                    for (int yl = 0; yl < ty; yl += 2) {
-                        const uint32_t o = accSeq + (uint32_t)(yl >> 1), a = o % g.na, ka = o / g.na;
-                        if (ka > 0) mbar_wait_warp(&aempty[a], (ka - 1) & 1, &s_abort, p.status);
-                        // image rows yl .. yl+hT (the last, for row yl+1 only, is skipped
-                        // when yl is the tile's last row)
-                        const int dmax = yl + 1 < ty ? p.hT : p.hT - 1;
-                        while (ready <= yl + dmax) {
-                            const uint32_t q = rowSeq + ready;
-                            mbar_wait_warp(&xfull[readySlot], (q / g.nx) & 1, &s_abort, p.status);
-                            ++ready;
-                            if (++readySlot == (uint32_t)g.nx) readySlot = 0;
-                        }
-                        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                        uint32_t s = (slot0 + yl) % g.nx;
-                        const uint32_t d = tmem + a * g.accCols;
+                const uint32_t nx = (uint32_t)g.nx, na = (uint32_t)g.na;
+                const uint32_t slot0 = rowSeq % nx;                             // slot of image row y0
+                // next image row to confirm (this tile's row `ready`), its slot and phase
+                int ready = 0;
+                uint32_t rSlot = slot0, rPhase = (rowSeq / nx) & 1;
+                // rows [ready, tested) were found complete by a look-ahead test
+                int tested = 0;
+                // stage of the current accumulator, how often the stage was used
+                // before (aK) and aK's parity
+                uint32_t aSlot = accSeq % na, aK = accSeq / na, aPhase = aK & 1;
+                bool aTested = false;
+                // confirms this tile's image rows up to `need` (waiting for those no test saw)
+                auto confirm_rows = [&](int need) {
+                    while (ready <= need) {
+                        if (ready >= tested)
+                            mbar_wait_lane(&xfull[rSlot], rPhase, &s_abort, p.status);
+                        ++ready;
+                        if (++rSlot == nx) { rSlot = 0; rPhase ^= 1u; }
+                    }
+                };
+                // tests the image rows (ready, need] after the confirmed ones, in order
+                auto test_rows = [&](int need) {
+                    int r = max(ready, tested);
+                    uint32_t s = rSlot, ph = rPhase;
+                    for (int k = ready; k < r; ++k) { if (++s == nx) { s = 0; ph ^= 1u; } }
+                    for (; r <= need && r < nrows; ++r) {
+                        if (!mbar_test(&xfull[s], ph)) break;
+                        tested = r + 1;
+                        if (++s == nx) { s = 0; ph ^= 1u; }
+                    }
+                };
+                auto next_acc = [&]() {
+                    if (++aSlot == na) { aSlot = 0; aPhase ^= 1u; ++aK; }
+                };
+                const int accPerTile = kPair ? (ty + 1) >> 1 : ty;
+                uint32_t ySlot = slot0;  // slot of image row y0 + yl
+                for (int ai = 0; ai < accPerTile; ++ai) {
+                    const int yl = kPair ? 2 * ai : ai;
+                    // this accumulator: its stage free, its image rows converted
+                    if (aK > 0 && !aTested)
+                        mbar_wait_lane(&aempty[aSlot], aPhase ^ 1u, &s_abort, p.status);
+                    const int dmax = kPair ? (yl + 1 < ty ? p.hT : p.hT - 1) : p.hT - 1;
+                    confirm_rows(yl + dmax);
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    // look-ahead for the next accumulator (results used after the MMAs)
+                    const uint32_t nSlot = aSlot + 1 == na ? 0u : aSlot + 1;
+                    const uint32_t nK = aSlot + 1 == na ? aK + 1 : aK;
+                    aTested = nK == 0 || mbar_test(&aempty[nSlot], (nK & 1u) ^ 1u);
+                    if (ai + 1 < accPerTile) {
+                        const int yn = kPair ? yl + 2 : yl + 1;
+                        const int dn = kPair ? (yn + 1 < ty ? p.hT : p.hT - 1) : p.hT - 1;
+                        test_rows(yn + dn);
+                    }
+                    uint32_t s = ySlot;
+                    const uint32_t d0 = tmem + aSlot * g.accCols;
+                    if (kPair) {
+                        // B window of image row d: blocks hT-d and hT-d+1 (see make_geom)
+                        const uint64_t bdescP = smem_desc(saddr(smem + g.offB), (uint32_t)((p.hT + 2) * g.nTpad * 16), 128);
+                        const uint32_t bBlk = (uint32_t)(g.nTpad * 16) >> 4;
+                        const uint32_t bChunkP = (uint32_t)(2 * (p.hT + 2) * g.nTpad * 16) >> 4;
                         for (int dd = 0; dd <= dmax; ++dd) {
                             const uint64_t ad = adesc0 + (uint64_t)(s * xStep);
                             const uint64_t bd = bdescP + (uint64_t)((p.hT - dd) * bBlk);
                             for (int c = 0; c < g.nK16; ++c)
-                                tc_mma_if(d, ad + 16u * c, bd + c * bChunkP, idesc,
-                                          (dd != 0 || c != 0) ? 1u : 0u, leader);
-                            if (++s == (uint32_t)g.nx) s = 0;
+                                tc_mma(d0, ad + 16u * c, bd + c * bChunkP, idesc,
+                                       (dd != 0 || c != 0) ? 1u : 0u);
+                            if (++s == nx) s = 0;
                         }
-                        tc_commit_if(&afull[a], leader);
-                        tc_commit_if(&xempty[(slot0 + yl) % g.nx], leader);  // image rows y0+yl, y0+yl+1 done
-                        if (yl + 1 < ty) tc_commit_if(&xempty[(slot0 + yl + 1) % g.nx], leader);
+                        tc_commit(&afull[aSlot]);
+                        tc_commit(&xempty[ySlot]);  // image rows y0+yl, y0+yl+1 done
+                        if (yl + 1 < ty) tc_commit(&xempty[ySlot + 1 == nx ? 0 : ySlot + 1]);
+                    } else {
+                        uint32_t d = d0;
+                        uint64_t bd = bdesc0;
+                        int inGroup = 0;
+                        for (int j = 0; j < p.hT; ++j) {
+                            const uint64_t ad = adesc0 + (uint64_t)(s * xStep);
+                            for (int c = 0; c < g.nK16; ++c)
+                                tc_mma(d, ad + 16u * c, bd + c * bChunk, idesc,
+                                       (inGroup != 0 || c != 0) ? 1u : 0u);
+                            bd += bRow;
+                            if (++s == nx) s = 0;
+                            if (++inGroup == g.G) { inGroup = 0; d += g.nTpad; }
+                        }
+                        tc_commit(&afull[aSlot]);
+                        tc_commit(&xempty[ySlot]);  // image row y0+yl is done
                     }
+                    next_acc();
+                    for (int k = 0; k < (kPair ? 2 : 1); ++k)
+                        if (++ySlot == nx) ySlot = 0;
                 }
-                for (int yl = 0; yl < ty && !kPair; ++yl) {
-                    const uint32_t o = accSeq + yl, a = o % g.na, ka = o / g.na;
-                    if (ka > 0) mbar_wait_warp(&aempty[a], (ka - 1) & 1, &s_abort, p.status);
-                    while (ready < yl + p.hT) {
-                        const uint32_t q = rowSeq + ready;
-                        mbar_wait_warp(&xfull[readySlot], (q / g.nx) & 1, &s_abort, p.status);
-                        ++ready;
-                        if (++readySlot == (uint32_t)g.nx) readySlot = 0;
-                    }
-                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    uint32_t s = (slot0 + yl) % g.nx;  // slot of image row y0+yl
-                    uint32_t d = tmem + a * g.accCols;
-                    uint64_t bd = bdesc0;
-                    int inGroup = 0;
-                    for (int j = 0; j < p.hT; ++j) {
-                        const uint64_t ad = adesc0 + (uint64_t)(s * xStep);
-                        for (int c = 0; c < g.nK16; ++c)
-                            tc_mma_if(d, ad + 16u * c, bd + c * bChunk, idesc,
-                                      (inGroup != 0 || c != 0) ? 1u : 0u, leader);
-                        bd += bRow;
-                        if (++s == (uint32_t)g.nx) s = 0;
-                        if (++inGroup == g.G) { inGroup = 0; d += g.nTpad; }
-                    }
-                    tc_commit_if(&afull[a], leader);
-                    tc_commit_if(&xempty[(slot0 + yl) % g.nx], leader);  // image row y0+yl is done
+                for (int rl = ty; rl < nrows; ++rl) {
+                    uint32_t e0 = (slot0 + (uint32_t)rl) % nx;
+                    tc_commit(&xempty[e0]);
                 }
-                for (int rl = ty; rl < nrows; ++rl) tc_commit_if(&xempty[(slot0 + rl) % g.nx], leader);
             }
             __syncwarp();
         } else {
