@@ -60,7 +60,8 @@ enum ncc_status_code {
     NCC_ERR_UNSUPPORTED = -2,  /* valid request outside the library's limits  */
     NCC_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed         */
     NCC_ERR_TIMEOUT = -4,      /* a kernel's bounded wait ran out (device)     */
-    NCC_ERR_NOMEM = -5         /* stream-ordered workspace allocation failed   */
+    NCC_ERR_NOMEM = -5,        /* stream-ordered workspace allocation failed   */
+    NCC_ERR_BOUNDS = -6        /* a debug build's index check failed (device)  */
 };
 
 /*
@@ -142,11 +143,13 @@ int ncc_sat_build_noalloc(const uint8_t *img, int W, int H, int64_t *S,
  *   S, Q device int64 [H][W]: must hold ncc_sat_build(img) output, ordered
  *        before this call (same stream, or an event).
  *   out  device fp32 [Oy][Ox], written completely; must not overlap inputs.
- * Kernel: the integer dot-product (dp4a) numerator.  A tensor-core
- * numerator (tcgen05, exact f16 products and fp32 sums) covers hT <= 16,
- * wT*hT <= 258, wT <= 126, W a multiple of 16 and 16-byte aligned img, S and
- * Q; it is selected with ncc_debug_set_path(NCC_PATH_TENSOR).  Both produce
- * the same integer sums; the coefficients agree to fp32 rounding.
+ * Kernels: the integer dot-product (dp4a) numerator, or -- for templates up
+ * to 65 pixels wide whose dp4a numerator would take at least 320 dp4a per
+ * output, ceil(wT/4)*hT (about 40x40 and up) -- a tensor-core numerator
+ * (tcgen05) that writes the sums over 64 consecutive shifts as one matrix
+ * product with a Toeplitz factor, from exact centered f16 operands (pixel and
+ * template value minus 128) accumulated in fp32 groups of at most 1024
+ * products.  Both produce the same integer sums and the same coefficients.
  * Returns NCC_OK, NCC_ERR_INVALID_ARG, NCC_ERR_UNSUPPORTED or NCC_ERR_CUDA.
  */
 int ncc_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl,

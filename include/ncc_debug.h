@@ -22,7 +22,12 @@ extern "C" {
  * publishes its look-back results, so every tile that depends on it waits
  * until its limit (timeout_ns; 0 restores the default of one second) runs
  * out and records NCC_ERR_TIMEOUT.  suppress_tile = -1 restores normal
- * operation.  Process-wide; not for concurrent use.
+ * operation.  In the debug build (libncc_gb300_debug.so, compiled with
+ * NCC_DEBUG), suppress_tile = -2 instead sends the table stores of tile 0
+ * one row width to the left, before the start of S and Q, where the build's
+ * index check must stop them and record NCC_ERR_BOUNDS; the regular build
+ * refuses -2.
+ * Process-wide; not for concurrent use.
  */
 int ncc_debug_set_fault(int suppress_tile, uint64_t timeout_ns);
 
@@ -41,7 +46,7 @@ int ncc_debug_fail_alloc(int count);
 enum ncc_path_code {
     NCC_PATH_NONE = 0,
     NCC_PATH_DP4A = 1,     /* single template, integer dot products         */
-    NCC_PATH_TENSOR = 2,   /* single template, tcgen05 tensor cores          */
+    /* 2 is not used (it named a tensor-core kernel that has been removed) */
     NCC_PATH_BANK = 3,     /* template bank, tcgen05 tensor cores            */
     NCC_PATH_TOEPLITZ = 4  /* single large template, tcgen05 Toeplitz product */
 };
@@ -50,9 +55,9 @@ enum ncc_path_code {
  * ncc_debug_set_path -- selects the single-template kernel that
  * ncc_correlate, ncc_correlate_moments and ncc_correlate_bank (for banks the
  * bank kernel does not take) use.  0 = automatic (the Toeplitz tensor-core
- * kernel for templates at least 48 pixels wide where it applies, else
- * dp4a), NCC_PATH_DP4A = dp4a, NCC_PATH_TENSOR = the row-window tensor-core
- * kernel, NCC_PATH_TOEPLITZ = the Toeplitz tensor-core kernel
+ * kernel where it applies and the dp4a numerator would take at least 320
+ * dp4a per output, ceil(wT/4)*hT -- about 40x40 and up -- else dp4a),
+ * NCC_PATH_DP4A = dp4a, NCC_PATH_TOEPLITZ = the Toeplitz tensor-core kernel
  * (NCC_ERR_UNSUPPORTED where the forced kernel does not apply).
  * Process-wide; not for concurrent use.
  * Returns NCC_OK, or NCC_ERR_INVALID_ARG for another value.

@@ -4,6 +4,12 @@ Each translation unit compiles in its own nvcc process (in parallel), then
 nvcc links them into one shared library with the CUDA runtime linked
 statically, so the library loads on a machine without a GPU driver (calls
 then fail with NCC_ERR_CUDA).
+
+build(debug=True) makes libncc_gb300_debug.so from the same sources with
+-DNCC_DEBUG: the kernels then check their hand-computed indices (shared
+memory, tensor-memory columns, operand descriptors, table and output
+addresses) and report a failed check as NCC_ERR_BOUNDS through the status
+word instead of making the access.
 """
 from __future__ import annotations
 
@@ -18,6 +24,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libncc_gb300.so")
+DEBUG_BUILD_DIR = os.path.join(PKG, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(PKG, "libncc_gb300_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -40,23 +48,30 @@ def _deps() -> list[str]:
         sorted(glob.glob(os.path.join(INCLUDE, "*.h"))) + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(debug: bool = False) -> bool:
+    lib = DEBUG_LIB_PATH if debug else LIB_PATH
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile every csrc/*.cu for sm_103a and link libncc_gb300.so."""
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          debug: bool = False) -> str:
+    """Compile every csrc/*.cu for sm_103a and link libncc_gb300.so (or, with
+    debug, libncc_gb300_debug.so with the device-side index checks)."""
+    lib = DEBUG_LIB_PATH if debug else LIB_PATH
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    if not force and up_to_date(debug):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if debug:
+        extra = extra + ["-DNCC_DEBUG"]
 
     def compile_one(src: str) -> tuple[str, str]:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *CFLAGS, *extra, "-c", src, "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
@@ -69,15 +84,24 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for _, log in results:
             if log:
                 print(log)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lrt", "-lpthread", "-ldl"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{res.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_all(force: bool = False) -> tuple[str, str]:
+    """The regular and the debug library, compiled side by side."""
+    with cf.ThreadPoolExecutor(max_workers=2) as ex:
+        a = ex.submit(build, force)
+        b = ex.submit(build, force, False, False, True)
+        return a.result(), b.result()
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="-v" in sys.argv,
+                debug="--debug" in sys.argv))

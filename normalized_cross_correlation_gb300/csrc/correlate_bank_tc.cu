@@ -293,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                                         (n >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2
                                   : (jb * g.nK16 + c) * g.nTpad * 32 + (k >> 3) * g.nTpad * 16 +
                                         (n >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2;
-            *reinterpret_cast<__half *>(smem + g.offB + off) = __float2half(v);
+            if (NCC_BOUNDS(off >= 0 && off + 2 <= g.bBytes, p.status))
+                *reinterpret_cast<__half *>(smem + g.offB + off) = __float2half(v);
         }
         const long long N = (long long)p.wT * p.hT;
         for (int n = tid; n < g.nTpad; n += kThreads) {
@@ -393,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                         h.y = bytes_to_h2(w0, 0x4342);
                         h.z = bytes_to_h2(w1, 0x4140);
                         h.w = bytes_to_h2(w1, 0x4342);
-                        *reinterpret_cast<uint4 *>(X + row * 16) = h;
+                        if (NCC_BOUNDS(slot < (uint32_t)g.nx && row * 16 + 16 <= g.xBytes, p.status))
+                            *reinterpret_cast<uint4 *>(X + row * 16) = h;
                     }
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -478,6 +480,14 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                         const uint32_t bBlk = (uint32_t)(g.nTpad * 16) >> 4;
                         const uint32_t bChunkP = (uint32_t)(2 * (p.hT + 2) * g.nTpad * 16) >> 4;
                         for (int dd = 0; dd <= dmax; ++dd) {
+                            // A slot in the ring; B blocks hT-dd and hT-dd+1 of hT+2;
+                            // N = 2*nTpad columns of this accumulator stage
+                            if (!NCC_BOUNDS(s < nx && p.hT - dd >= 0 && p.hT - dd + 1 <= p.hT + 1 &&
+                                                (aSlot + 1) * (uint32_t)g.accCols <= (uint32_t)g.tmemCols,
+                                            p.status)) {
+                                if (++s == nx) s = 0;
+                                continue;
+                            }
                             const uint64_t ad = adesc0 + (uint64_t)(s * xStep);
                             const uint64_t bd = bdescP + (uint64_t)((p.hT - dd) * bBlk);
                             for (int c = 0; c < g.nK16; ++c)
@@ -494,6 +504,8 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                         int inGroup = 0;
                         for (int j = 0; j < p.hT; ++j) {
                             const uint64_t ad = adesc0 + (uint64_t)(s * xStep);
+                            if (NCC_BOUNDS(s < nx && d + (uint32_t)g.nTpad <= tmem + (aSlot + 1) * (uint32_t)g.accCols,
+                                           p.status))
                             for (int c = 0; c < g.nK16; ++c)
                                 tc_mma(d, ad + 16u * c, bd + c * bChunk, idesc,
                                        (inGroup != 0 || c != 0) ? 1u : 0u);
@@ -560,7 +572,11 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                 mbar_wait_warp(&afull[a], ka & 1, &s_abort, p.status);
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const size_t obase = (size_t)y * p.Ox + x;
-                if (kMoments && xin && (kPair || ch == 0)) {
+                // lanes whose output (or window) a check finds outside the
+                // map store nothing; the warp-wide loads still run in step
+                const bool xok = xin && NCC_BOUNDS(y < p.Oy && x < p.Ox && y + p.hT - 1 < p.H &&
+                                                       x + p.wT - 1 < p.W, p.status);
+                if (kMoments && xok && (kPair || ch == 0)) {
                     p.sumI[obase] = sI;
                     p.sumI2[obase] = sI2;
                 }
@@ -581,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                             for (int i = 0; i < 32; ++i) v[i] += __float2uint_rn(__uint_as_float(w[i]));
                         }
                     }
-                    if (!xin) continue;
+                    if (!xok) continue;
                     if constexpr (!kMoments && kOneGroup) {
                         // r = (N*SumIT - SumI*SumT) / sqrt(vI*vT) with the numerator
                         // exact up to its last rounding: p2 = fl(SumI*SumT), e2 its

@@ -502,6 +502,8 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
             for (int q = 0; q < 2; ++q) {
                 const int o = (h + 2 * q) * segWords;
                 const uint32_t *St = b + o, *Sb = b + box + o, *Qt = b + 2 * box + o, *Qb = b + 3 * box + o;
+                // both corners inside the staged segment, the segment inside its box
+                if (!NCC_BOUNDS(cl >= 0 && cr < segWords && o + segWords <= box, p.status)) continue;
                 sIv[q] = Sb[cr] - St[cr] - Sb[cl] + St[cl];
                 sI2v[q] = Qb[cr] - Qt[cr] - Qb[cl] + Qt[cl];
             }
@@ -533,6 +535,8 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
             const unsigned sumIT = sIT[row * kOutW + xs];
             const size_t o = (size_t)y * p.Ox + x;
             float *const op = outRow + (q ? ox2 : (size_t)0);
+            // the output inside the map; the stepped row pointer at its address
+            if (!NCC_BOUNDS(y < p.Oy && x < p.Ox && (kMoments || op == p.out + o), p.status)) continue;
             if (kMoments) {
                 p.sumI[o] = (long long)sI;
                 p.sumI2[o] = (long long)sI2;
@@ -682,6 +686,11 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
         for (int i = 0; i < kDirRows / 2; ++i) {
             const int r = h + 2 * i, row = yb + r, y = y0 + row;
             if (kFull || (y < p.Oy && x < p.Ox)) {
+                // the prefix entries inside the pass's buffers; the output in the map
+                if (!NCC_BOUNDS(xo + p.wT < cP && y < p.Oy && x < p.Ox &&
+                                    (kMoments || outPass + (size_t)i * ox2 == p.out + (size_t)y * p.Ox + x),
+                                p.status))
+                    continue;
                 const uint32_t sI = P1[r * cP + xo + p.wT] - P1[r * cP + xo];
                 const uint32_t sI2 = P2[r * cP + xo + p.wT] - P2[r * cP + xo];
                 const unsigned sumIT = sIT[row * kOutW + xs];

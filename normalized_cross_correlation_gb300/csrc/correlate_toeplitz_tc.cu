@@ -389,7 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1) toeplitz_tc_kernel(const TParams 
                     h.z = bytes_to_centered_h2(v[k].x, 0x4243);
                     h.w = bytes_to_centered_h2(v[k].x, 0x4041);
                     if (!inside) h = make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4 *>(A + (size_t)qq * g.R * 16 + (size_t)r * 16) = h;
+                    const size_t off = (size_t)qq * g.R * 16 + (size_t)r * 16;
+                    if (NCC_BOUNDS(off + 16 <= (size_t)g.aBytes, p.status))
+                        *reinterpret_cast<uint4 *>(A + off) = h;
                 }
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -410,6 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1) toeplitz_tc_kernel(const TParams 
                 const int rows = min(g.hg, p.hT - j0);
                 for (int e = pt; e < rows * g.hRows; e += kPT) {
                     const int jj = e / g.hRows, t = e - jj * g.hRows;
+                    if (!NCC_BOUNDS((j0 + jj) * g.pLen + t + 8 <= p.hT * g.pLen &&
+                                        gs * g.hg + jj < g.nH, p.status))
+                        continue;
                     const uint16_t *Pj = P + (j0 + jj) * g.pLen;
                     uint4 h;
                     h.x = (uint32_t)Pj[t] | ((uint32_t)Pj[t + 1] << 16);
@@ -457,6 +462,12 @@ __global__ void __launch_bounds__(kThreads, 1) toeplitz_tc_kernel(const TParams 
                     const int rows = min(g.hg, p.hT - j0);
                     for (int jj = 0; jj < rows; ++jj) {
                         const int j = j0 + jj;
+                        // A rows j..j+127 of the tile, Hankel rows up to
+                        // 16*(nK16-1)+71, accumulator columns of the group
+                        if (!NCC_BOUNDS(j + kM <= g.R && (int)(gs * g.hg) + jj < g.nH &&
+                                            16 * (nK16 - 1) + 72 <= g.hRows &&
+                                            (accGroup + 1) * kN <= kAccCols, p.status))
+                            continue;
                         const uint32_t d = dTile + (uint32_t)(accGroup * kN);
                         const uint64_t a = aTile + (uint64_t)j;  // 16 bytes per template row
                         const uint64_t b = hDesc0 + (uint64_t)((gs * g.hg + jj) * hRow);
@@ -539,6 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1) toeplitz_tc_kernel(const TParams 
                 for (int i = 0; i < 16; ++i) acc[i] = 0;
                 for (int gi = 0; gi < g.nG; ++gi) {
                     uint32_t v[16];
+                    // a warp-uniform check: the load is a whole-warp instruction
+                    if (!NCC_BOUNDS(gi * kN + 32 * hf + 16 * half + 16 <= kAccCols, p.status)) continue;
                     tc_ld16(tmem + laneBase + ab * kAccCols + (uint32_t)(gi * kN + 32 * hf + 16 * half), v);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
@@ -562,6 +575,9 @@ __global__ void __launch_bounds__(kThreads, 1) toeplitz_tc_kernel(const TParams 
                 const int y = y0 + 32 * qd + r;
                 const int c = X[r * 33 + lane];
                 if (!xin) continue;
+                if (!NCC_BOUNDS(y + p.hT - 1 < p.H && xr < p.W && (size_t)y * p.Ox + x <
+                                    (size_t)p.Oy * p.Ox, p.status))
+                    continue;
                 const unsigned *Sb = reinterpret_cast<const unsigned *>(p.S + (size_t)(y + p.hT - 1) * W);
                 const unsigned *Qb = reinterpret_cast<const unsigned *>(p.Q + (size_t)(y + p.hT - 1) * W);
                 uint32_t sI = __ldg(Sb + 2 * (size_t)xr), sI2 = __ldg(Qb + 2 * (size_t)xr);

@@ -38,8 +38,13 @@ void set_last_path(int path) {
 }
 
 constexpr int kMaxW = 66051;  // 66051 * 255^2 < 2^32: a row's running sum of squares fits uint32
-// Narrowest template that automatic selection gives the Toeplitz kernel.
-constexpr int kToeplitzMinWidth = 48;
+// Automatic selection gives a single template to the Toeplitz kernel when
+// the dp4a numerator would take at least this many dp4a per output
+// (ceil(wT/4) * hT).  Measured on this GPU, the Toeplitz kernel's time hardly
+// depends on the template (its box-sum epilogue binds) while dp4a's grows
+// with it; they cross between 32x32 (256 per output: dp4a faster at every
+// image size tried) and 40x40 (400: the Toeplitz kernel faster).
+constexpr long long kToeplitzMinDp4a = 320;
 constexpr long long kMaxN = 66051;  // wT*hT*255^2 < 2^32: SumIT fits uint32
 
 int status_ptr(int **out) {
@@ -154,10 +159,10 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
     // Automatic selection: the Toeplitz tensor-core product for wide
     // templates, whose numerator dominates; dp4a otherwise.
     const bool toeplitz = ncc::corr_toeplitz_supported(wT, hT) &&
-                          (path == NCC_PATH_TOEPLITZ || (path == 0 && wT >= kToeplitzMinWidth));
+                          (path == NCC_PATH_TOEPLITZ ||
+                           (path == 0 && (long long)((wT + 3) / 4) * hT >= kToeplitzMinDp4a));
     if (path == NCC_PATH_TOEPLITZ && !toeplitz) return NCC_ERR_UNSUPPORTED;
-    if (path != NCC_PATH_TENSOR && !toeplitz && !ncc::corr_dp4a_supported(wT, hT))
-        return NCC_ERR_UNSUPPORTED;
+    if (!toeplitz && !ncc::corr_dp4a_supported(wT, hT)) return NCC_ERR_UNSUPPORTED;
     int used = NCC_PATH_NONE;
     for (int t = 0; t < nT; ++t) {
         ncc::CorrArgs a;
@@ -174,15 +179,7 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
         a.overlap_prev = after_sat && t == 0;
         a.direct = direct;
         cudaError_t e = cudaErrorNotSupported;
-        // Automatic selection takes the dp4a kernel: on the 4096x4096 /
-        // 16x16 workload it measures faster than the tensor-core kernel
-        // (about 200 vs 250 us), whose tiny N = 16 MMAs leave it bound by
-        // pipeline hand-off latency rather than by the tensor pipe.
-        if (path == NCC_PATH_TENSOR && !a.overlap_prev && ncc::corr_tc_supported(a)) {
-            e = ncc::corr_tc_launch(a, stream);
-            if (e == cudaSuccess) used = NCC_PATH_TENSOR;
-        }
-        if (e == cudaErrorNotSupported && toeplitz) {
+        if (toeplitz) {
             // plain stream order: behind the table build the early start
             // measured slower for this kernel (8192x8192, 64x64: 2.19 ms per
             // image against 1.87 ms as two calls), its CTAs taking whole SMs
@@ -191,7 +188,7 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
             if (e == cudaSuccess) used = NCC_PATH_TOEPLITZ;
         }
         if (e == cudaErrorNotSupported) {
-            if (path == NCC_PATH_TENSOR || path == NCC_PATH_TOEPLITZ) return NCC_ERR_UNSUPPORTED;
+            if (path == NCC_PATH_TOEPLITZ) return NCC_ERR_UNSUPPORTED;
             e = ncc::corr_dp4a_launch(a, stream);
             if (e == cudaSuccess) used = NCC_PATH_DP4A;
         }
@@ -350,7 +347,7 @@ int ncc_match(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int
     }
     // the overlap only behind the fused builder, which lets its dependents start
     return run_correlate(img, W, H, tmpl, wT, hT, nT, S, Q, out, nullptr, nullptr, nullptr,
-                         reinterpret_cast<cudaStream_t>(stream), path != NCC_PATH_TENSOR);
+                         reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 int ncc_match_host(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT,
@@ -432,6 +429,7 @@ const char *ncc_status_string(int status) {
         case NCC_ERR_CUDA: return "CUDA runtime error";
         case NCC_ERR_TIMEOUT: return "look-back wait timed out";
         case NCC_ERR_NOMEM: return "device workspace allocation failed";
+        case NCC_ERR_BOUNDS: return "index check failed (debug build)";
         default: return "unknown status";
     }
 }
@@ -439,8 +437,7 @@ const char *ncc_status_string(int status) {
 int ncc_version(void) { return (0 << 16) | 1; }
 
 int ncc_debug_set_path(int path) {
-    if (path != 0 && path != NCC_PATH_DP4A && path != NCC_PATH_TENSOR && path != NCC_PATH_TOEPLITZ)
-        return NCC_ERR_INVALID_ARG;
+    if (path != 0 && path != NCC_PATH_DP4A && path != NCC_PATH_TOEPLITZ) return NCC_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(g_mutex);
     g_path = path;
     return NCC_OK;
@@ -458,7 +455,11 @@ int ncc_debug_fail_alloc(int count) {
 }
 
 int ncc_debug_set_fault(int suppress_tile, uint64_t timeout_ns) {
+#ifdef NCC_DEBUG
+    if (suppress_tile < -2) return NCC_ERR_INVALID_ARG;  // -2: the index-check test
+#else
     if (suppress_tile < -1) return NCC_ERR_INVALID_ARG;
+#endif
     std::lock_guard<std::mutex> lock(g_mutex);
     g_fault_tile = suppress_tile;
     g_timeout_ns = timeout_ns ? timeout_ns : 1000000000ull;

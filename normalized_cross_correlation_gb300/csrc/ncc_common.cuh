@@ -42,6 +42,17 @@ __device__ __forceinline__ void record_status(int *status, int code) {
     atomicCAS(status, 0, code);
 }
 
+// Index checks of the debug build (compiled with -DNCC_DEBUG): NCC_BOUNDS(c,
+// status) is true when c holds; when it does not, it records NCC_ERR_BOUNDS
+// in the status word and is false, so the caller skips the access.  In the
+// regular build it is the constant true and costs nothing.
+#ifdef NCC_DEBUG
+#define NCC_BOUNDS(cond, status) \
+    ((cond) ? true : (::ncc::record_status((status), NCC_ERR_BOUNDS), false))
+#else
+#define NCC_BOUNDS(cond, status) true
+#endif
+
 // Look-back flag states (section 15.8's three-state protocol).
 enum : unsigned { FLAG_EMPTY = 0u, FLAG_AGGREGATE = 1u, FLAG_PREFIX = 2u };
 
@@ -173,11 +184,6 @@ bool corr_dp4a_supported(int wT, int hT);
 // The same with direct window moments (CorrArgs::direct): wT <= 129.
 bool corr_dp4a_direct_supported(int wT, int hT);
 cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream);
-// The same on the tensor cores (tcgen05; hT <= 16, wT*hT <= 258, wT <= 126,
-// W a multiple of 16, 16-byte aligned img, S and Q).  Returns
-// cudaErrorNotSupported, launching nothing, when the shape does not fit.
-bool corr_tc_supported(const CorrArgs &a);
-cudaError_t corr_tc_launch(const CorrArgs &a, cudaStream_t stream);
 // The same as a Toeplitz matrix product on the tensor cores (tcgen05, exact
 // centered f16 operands, fp32 accumulation in groups of at most 1024
 // products): wT <= 65 and a tile that fits two CTAs per SM.  Honours

@@ -437,7 +437,7 @@ sat_build_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__rest
             }
             const uint64_t rowV = (uint64_t)rowI | ((uint64_t)rowQ << kRowQShift);
             uint64_t *rowMine = ws.row + (size_t)tile * kTileH + pt;
-            if (publish)
+            if (publish && NCC_BOUNDS(tile < ntiles && pt < kTileH, status))
                 st_relaxed_u64(rowMine, make_word(epoch, tx == 0 ? FLAG_PREFIX : FLAG_AGGREGATE, rowV));
 
             // 3. row carry by look-back to the left.  The column look-back
@@ -547,7 +547,7 @@ sat_build_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__rest
                 }
                 uint64_t *mine = ws.col + (size_t)tile * kColWords + c;
                 const bool early = colS.done && colQ.done;  // ty == 0 included
-                if (publish) {
+                if (publish && NCC_BOUNDS(tile < ntiles && c + kTileW < kColWords, status)) {
                     const uint32_t state = early ? FLAG_PREFIX : FLAG_AGGREGATE;
                     const uint64_t b0 = early ? colS.acc : 0ull, b1 = early ? colQ.acc : 0ull;
                     st_relaxed_u64(mine, make_word(epoch, state, b0 + (uint64_t)agg[0]));
@@ -612,7 +612,14 @@ sat_build_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__rest
             const int tile = S_.tile;
             if (tile < 0) break;  // done or aborted: no release, the producer stopped too
             const int tx = tile % ntx, ty = tile / ntx;
-            const int xl = tx * kTileW + 4 * lane;
+            int xl = tx * kTileW + 4 * lane;
+#ifdef NCC_DEBUG
+            // debug builds only: fault_tile == -2 sends tile 0's stores one
+            // row width to the left (before the start of S and Q), for the
+            // test that the check below catches it: the stores are skipped
+            // and NCC_ERR_BOUNDS is recorded
+            if (fault_tile == -2 && tile == 0) xl -= W;
+#endif
             const int ps = S_.pix;
             long long runI[4], runQ[4];
 #pragma unroll
@@ -645,6 +652,7 @@ sat_build_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__rest
                     }
                     if (y >= H) continue;
                     const size_t o = (size_t)y * W + xl;
+                    if (!NCC_BOUNDS(tile < ntiles && xl >= 0, status)) continue;
                     if (kStore == 2 && xl + 3 < W) {
                         st_v4_b64(S + o, runI[0], runI[1], runI[2], runI[3]);
                         st_v4_b64(Q + o, runQ[0], runQ[1], runQ[2], runQ[3]);

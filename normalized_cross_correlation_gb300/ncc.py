@@ -21,6 +21,7 @@ NCC_ERR_UNSUPPORTED = -2
 NCC_ERR_CUDA = -3
 NCC_ERR_TIMEOUT = -4
 NCC_ERR_NOMEM = -5
+NCC_ERR_BOUNDS = -6
 
 NCC_SAT_FUSED = 0      # the single-pass tiled look-back (ncc_sat_build)
 NCC_SAT_NAIVE = 1      # one thread per row, then one thread per column
@@ -43,7 +44,9 @@ class NccError(RuntimeError):
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    """The library to load: the regular build, or the build with device-side
+    index checks when NCC_GB300_LIBRARY=debug is set in the environment."""
+    return _build.DEBUG_LIB_PATH if os.environ.get("NCC_GB300_LIBRARY") == "debug" else _build.LIB_PATH
 
 
 def lib() -> ctypes.CDLL:
@@ -366,7 +369,7 @@ def ncc_debug_fail_alloc(count: int) -> None:
     _check(lib().ncc_debug_fail_alloc(int(count)), "ncc_debug_fail_alloc")
 
 
-NCC_PATH_NONE, NCC_PATH_DP4A, NCC_PATH_TENSOR, NCC_PATH_BANK, NCC_PATH_TOEPLITZ = 0, 1, 2, 3, 4
+NCC_PATH_NONE, NCC_PATH_DP4A, NCC_PATH_BANK, NCC_PATH_TOEPLITZ = 0, 1, 3, 4
 
 
 def ncc_debug_set_path(path: int) -> None:

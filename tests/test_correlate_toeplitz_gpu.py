@@ -118,14 +118,18 @@ def test_toeplitz_zero_variance_and_negated_crop(toeplitz):
     assert ncc.ncc_sync_status() == 0
 
 
-def test_automatic_selection_takes_toeplitz_for_wide_templates(ncc):
+def test_automatic_selection_takes_toeplitz_for_large_templates(ncc):
+    """Toeplitz from ceil(wT/4)*hT >= 320 dp4a per output (40x40 and up),
+    dp4a below (32x32, and wide but short templates)."""
     w = inputs.random_case(5, 300, 200, 64, 64, nT=1, n_crops=1)
     dimg = to_dev(w.image)
     S, Q = ncc.ncc_sat_build(dimg)
-    ncc.ncc_correlate(dimg, to_dev(w.templates[0]), S, Q)
-    assert ncc.ncc_debug_last_path() == ncc.NCC_PATH_TOEPLITZ
-    ncc.ncc_correlate(dimg, to_dev(w.templates[0][:, :16]), S, Q)
-    assert ncc.ncc_debug_last_path() == ncc.NCC_PATH_DP4A
+    T = w.templates[0]
+    for tmpl, path in ((T, ncc.NCC_PATH_TOEPLITZ), (T[:40, :40], ncc.NCC_PATH_TOEPLITZ),
+                       (T[:32, :32], ncc.NCC_PATH_DP4A), (T[:16, :], ncc.NCC_PATH_DP4A),
+                       (T[:, :16], ncc.NCC_PATH_DP4A)):
+        ncc.ncc_correlate(dimg, to_dev(tmpl), S, Q)
+        assert ncc.ncc_debug_last_path() == path, tmpl.shape
     assert ncc.ncc_sync_status() == 0
 
 

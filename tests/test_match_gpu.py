@@ -87,22 +87,6 @@ def test_headline_size_on_a_side_stream_repeatedly(ncc):
             np.testing.assert_array_equal(out.cpu().numpy(), r0)
 
 
-def test_match_on_the_tensor_path_takes_no_overlap(ncc):
-    """With the tensor-core single-template kernel selected (it has no grid
-    dependency wait), ncc_match launches it in plain stream order."""
-    w = inputs.random_case(99, 512, 256, 16, 16, nT=1, n_crops=1)
-    dimg, dt = to_dev(w.image), to_dev(w.templates)
-    _, _, r0 = separate(ncc, dimg, dt)
-    ncc.ncc_debug_set_path(ncc.NCC_PATH_TENSOR)
-    try:
-        S, Q, r = ncc.ncc_match(dimg, dt)
-        assert ncc.ncc_sync_status() == 0
-        assert ncc.ncc_debug_last_path() == ncc.NCC_PATH_TENSOR
-    finally:
-        ncc.ncc_debug_set_path(0)
-    np.testing.assert_allclose(r.cpu().numpy(), r0, rtol=0, atol=TOL)
-
-
 @pytest.mark.parametrize("W,H,wT,hT,nT,pinned", [
     (1024, 600, 16, 16, 1, True), (1024, 600, 16, 16, 1, False),
     (523, 300, 7, 5, 1, True), (640, 480, 16, 16, 4, True), (640, 480, 16, 16, 4, False),
