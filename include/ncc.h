@@ -149,8 +149,15 @@ int ncc_sat_build_noalloc(const uint8_t *img, int W, int H, int64_t *S,
  * (tcgen05) that writes the sums over 64 consecutive shifts as one matrix
  * product with a Toeplitz factor, from exact centered f16 operands (pixel and
  * template value minus 128) accumulated in fp32 groups of at most 1024
- * products.  Both produce the same integer sums and the same coefficients.
- * Returns NCC_OK, NCC_ERR_INVALID_ARG, NCC_ERR_UNSUPPORTED or NCC_ERR_CUDA.
+ * products; for wider templates (up to 224 x 224 and 30000 pixels) past the
+ * same dp4a count, a numerator from number-theoretic transforms of 256 x 256
+ * image tiles (section 15.8's FFT numerator, computed modulo the prime
+ * 998244353, which makes it exact; centered values as above), which
+ * allocates the template's 512 KB spectrum from the library's stream-ordered
+ * pool for the duration of the call.  All produce the same integer sums and
+ * the same coefficients.
+ * Returns NCC_OK, NCC_ERR_INVALID_ARG, NCC_ERR_UNSUPPORTED, NCC_ERR_NOMEM
+ * (the spectrum could not be allocated) or NCC_ERR_CUDA.
  */
 int ncc_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl,
                   int wT, int hT, const int64_t *S, const int64_t *Q,

@@ -35,7 +35,7 @@ int ncc_debug_set_fault(int suppress_tile, uint64_t timeout_ns);
  * ncc_debug_fail_alloc -- test hook for allocation failure.  The next
  * `count` device allocations the library makes (the SAT builder's look-back
  * workspace when it is first allocated or grown, the host-buffer path's
- * device buffers) fail as on an exhausted device, so the calls that need
+ * device buffers, the transform kernel's template spectrum) fail as on an exhausted device, so the calls that need
  * them return NCC_ERR_NOMEM and launch nothing.  count = 0 cancels the
  * failures still pending.  Process-wide; not for concurrent use.
  * Returns NCC_OK, or NCC_ERR_INVALID_ARG for a negative count.
@@ -48,19 +48,19 @@ enum ncc_path_code {
     NCC_PATH_DP4A = 1,     /* single template, integer dot products         */
     /* 2 is not used (it named a tensor-core kernel that has been removed) */
     NCC_PATH_BANK = 3,     /* template bank, tcgen05 tensor cores            */
-    NCC_PATH_TOEPLITZ = 4  /* single large template, tcgen05 Toeplitz product */
+    NCC_PATH_TOEPLITZ = 4, /* single large template, tcgen05 Toeplitz product */
+    NCC_PATH_NTT = 5       /* single large template, number-theoretic transforms */
 };
 
 /*
  * ncc_debug_set_path -- selects the single-template kernel that
- * ncc_correlate, ncc_correlate_moments and ncc_correlate_bank (for banks the
- * bank kernel does not take) use.  0 = automatic (the Toeplitz tensor-core
- * kernel where it applies and the dp4a numerator would take at least 320
- * dp4a per output, ceil(wT/4)*hT -- about 40x40 and up -- else dp4a),
- * NCC_PATH_DP4A = dp4a, NCC_PATH_TOEPLITZ = the Toeplitz tensor-core kernel
- * (NCC_ERR_UNSUPPORTED where the forced kernel does not apply).
- * Process-wide; not for concurrent use.
- * Returns NCC_OK, or NCC_ERR_INVALID_ARG for another value.
+ * ncc_correlate, ncc_correlate_moments, ncc_match and ncc_correlate_bank (for
+ * banks the bank kernel does not take) use.  0 = automatic (see
+ * ncc_correlate in ncc.h), NCC_PATH_DP4A = dp4a, NCC_PATH_TOEPLITZ = the
+ * Toeplitz tensor-core kernel, NCC_PATH_NTT = the number-theoretic-transform
+ * kernel; a forced kernel that does not apply to the template's shape makes
+ * the call return NCC_ERR_UNSUPPORTED.  Process-wide; not for concurrent
+ * use.  Returns NCC_OK, or NCC_ERR_INVALID_ARG for another value.
  */
 int ncc_debug_set_path(int path);
 

@@ -45,6 +45,9 @@ constexpr int kMaxW = 66051;  // 66051 * 255^2 < 2^32: a row's running sum of sq
 // with it; they cross between 32x32 (256 per output: dp4a faster at every
 // image size tried) and 40x40 (400: the Toeplitz kernel faster).
 constexpr long long kToeplitzMinDp4a = 320;
+// Templates too wide for the Toeplitz kernel go to the transform kernel
+// from the same dp4a count on.
+constexpr long long kNttMinDp4a = 320;
 constexpr long long kMaxN = 66051;  // wT*hT*255^2 < 2^32: SumIT fits uint32
 
 int status_ptr(int **out) {
@@ -129,6 +132,7 @@ int check_direct(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, 
 int to_status(cudaError_t e) {
     if (e == cudaSuccess) return NCC_OK;
     if (e == cudaErrorMemoryAllocation) return NCC_ERR_NOMEM;
+    if (e == cudaErrorNotSupported) return NCC_ERR_UNSUPPORTED;
     return NCC_ERR_CUDA;
 }
 
@@ -156,13 +160,23 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
         return rc;
     }
     if (direct) path = NCC_PATH_DP4A;  // the direct moments exist on the dp4a kernel only
-    // Automatic selection: the Toeplitz tensor-core product for wide
-    // templates, whose numerator dominates; dp4a otherwise.
-    const bool toeplitz = ncc::corr_toeplitz_supported(wT, hT) &&
-                          (path == NCC_PATH_TOEPLITZ ||
-                           (path == 0 && (long long)((wT + 3) / 4) * hT >= kToeplitzMinDp4a));
-    if (path == NCC_PATH_TOEPLITZ && !toeplitz) return NCC_ERR_UNSUPPORTED;
-    if (!toeplitz && !ncc::corr_dp4a_supported(wT, hT)) return NCC_ERR_UNSUPPORTED;
+    // The single-template kernel: forced, or automatically the Toeplitz
+    // tensor-core product for wide templates, whose numerator dominates, the
+    // transform kernel for templates wider than that, dp4a otherwise.
+    const long long dp4aPerOutput = (long long)((wT + 3) / 4) * hT;
+    int kernel = NCC_PATH_DP4A;
+    if (path == NCC_PATH_TOEPLITZ || path == NCC_PATH_NTT) {
+        const bool ok = path == NCC_PATH_TOEPLITZ ? ncc::corr_toeplitz_supported(wT, hT)
+                                                  : ncc::corr_ntt_supported(wT, hT);
+        if (!ok) return NCC_ERR_UNSUPPORTED;
+        kernel = path;
+    } else if (path == 0) {
+        if (ncc::corr_toeplitz_supported(wT, hT) && dp4aPerOutput >= kToeplitzMinDp4a)
+            kernel = NCC_PATH_TOEPLITZ;
+        else if (ncc::corr_ntt_supported(wT, hT) && dp4aPerOutput >= kNttMinDp4a)
+            kernel = NCC_PATH_NTT;
+    }
+    if (kernel == NCC_PATH_DP4A && !ncc::corr_dp4a_supported(wT, hT)) return NCC_ERR_UNSUPPORTED;
     int used = NCC_PATH_NONE;
     for (int t = 0; t < nT; ++t) {
         ncc::CorrArgs a;
@@ -179,16 +193,19 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
         a.overlap_prev = after_sat && t == 0;
         a.direct = direct;
         cudaError_t e = cudaErrorNotSupported;
-        if (toeplitz) {
+        if (kernel == NCC_PATH_TOEPLITZ) {
             // plain stream order: behind the table build the early start
             // measured slower for this kernel (8192x8192, 64x64: 2.19 ms per
             // image against 1.87 ms as two calls), its CTAs taking whole SMs
             a.overlap_prev = false;
             e = ncc::corr_toeplitz_launch(a, stream);
-            if (e == cudaSuccess) used = NCC_PATH_TOEPLITZ;
+        } else if (kernel == NCC_PATH_NTT) {
+            a.overlap_prev = false;
+            e = ncc::corr_ntt_launch(a, stream);
         }
-        if (e == cudaErrorNotSupported) {
-            if (path == NCC_PATH_TOEPLITZ) return NCC_ERR_UNSUPPORTED;
+        if (e == cudaSuccess && kernel != NCC_PATH_DP4A) used = kernel;
+        if (e == cudaErrorNotSupported || kernel == NCC_PATH_DP4A) {
+            if (path == NCC_PATH_TOEPLITZ || path == NCC_PATH_NTT) return NCC_ERR_UNSUPPORTED;
             e = ncc::corr_dp4a_launch(a, stream);
             if (e == cudaSuccess) used = NCC_PATH_DP4A;
         }
@@ -437,7 +454,8 @@ const char *ncc_status_string(int status) {
 int ncc_version(void) { return (0 << 16) | 1; }
 
 int ncc_debug_set_path(int path) {
-    if (path != 0 && path != NCC_PATH_DP4A && path != NCC_PATH_TOEPLITZ) return NCC_ERR_INVALID_ARG;
+    if (path != 0 && path != NCC_PATH_DP4A && path != NCC_PATH_TOEPLITZ && path != NCC_PATH_NTT)
+        return NCC_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(g_mutex);
     g_path = path;
     return NCC_OK;

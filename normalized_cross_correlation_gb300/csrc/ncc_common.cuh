@@ -190,6 +190,13 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream);
 // CorrArgs::overlap_prev; no direct moments.
 bool corr_toeplitz_supported(int wT, int hT);
 cudaError_t corr_toeplitz_launch(const CorrArgs &a, cudaStream_t stream);
+// The same with the numerator from number-theoretic transforms of 256 x 256
+// tiles (exact modulo a prime): wT, hT <= 224 and wT * hT <= 30000.  Plain
+// stream order; no direct moments.  Allocates the template's spectrum
+// (512 KB) from the library's stream-ordered pool for the duration of the
+// call.
+bool corr_ntt_supported(int wT, int hT);
+cudaError_t corr_ntt_launch(const CorrArgs &a, cudaStream_t stream);
 
 // Template-bank correlation on the tensor cores (tcgen05, f16 operands,
 // fp32 accumulation; exact while wT*hT*255^2 < 2^24).

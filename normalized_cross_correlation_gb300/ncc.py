@@ -369,7 +369,7 @@ def ncc_debug_fail_alloc(count: int) -> None:
     _check(lib().ncc_debug_fail_alloc(int(count)), "ncc_debug_fail_alloc")
 
 
-NCC_PATH_NONE, NCC_PATH_DP4A, NCC_PATH_BANK, NCC_PATH_TOEPLITZ = 0, 1, 3, 4
+NCC_PATH_NONE, NCC_PATH_DP4A, NCC_PATH_BANK, NCC_PATH_TOEPLITZ, NCC_PATH_NTT = 0, 1, 3, 4, 5
 
 
 def ncc_debug_set_path(path: int) -> None:
