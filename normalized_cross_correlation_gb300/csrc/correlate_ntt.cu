@@ -183,7 +183,9 @@ __device__ __forceinline__ void stage_tile(const NttParams &p, int ty0, int tx0,
 // The epilogue of one half of a tile's output rows (u0 = 0 or 128): the
 // centered correlations C sit in the buffer, row u - u0, logical column
 // x - tx0; a warp takes a row, its lanes consecutive shifts (coalesced box
-// sums and stores).
+// sums and stores).  The table reads of four 32-shift chunks are issued
+// before any is used; their addresses are clamped into the row, so every
+// read is in bounds and only the stores are conditional.
 template <bool kMoments>
 __device__ __forceinline__ void epilogue_half(const NttParams &p, const ntt::Tile &t, int ty0, int tx0,
                                               int u0, long long N, unsigned sT, uint32_t cT,
@@ -198,44 +200,54 @@ __device__ __forceinline__ void epilogue_half(const NttParams &p, const ntt::Til
         const unsigned *Qb = reinterpret_cast<const unsigned *>(p.Q + (size_t)(y + p.hT - 1) * W);
         const unsigned *St = reinterpret_cast<const unsigned *>(p.S + (size_t)(y > 0 ? y - 1 : 0) * W);
         const unsigned *Qt = reinterpret_cast<const unsigned *>(p.Q + (size_t)(y > 0 ? y - 1 : 0) * W);
+        const uint32_t ym = y > 0 ? 0xffffffffu : 0u;
         const uint32_t *brow = t.buf + rr * ntt::kStride;
-#pragma unroll 1
-        for (int xl = lane; xl < cols; xl += 32) {
-            const int x = tx0 + xl, xlft = x - 1, xr = x + p.wT - 1;
-            if (!NCC_BOUNDS(y + p.hT - 1 < p.H && xr < p.W && (size_t)y * p.Ox + x < (size_t)p.Oy * p.Ox,
-                            p.status))
-                continue;
-            const int32_t c = (int32_t)brow[ntt::swz(xl)];
-            // box sums from the low 32 bits of S and Q (below 2^32, so the
-            // wrapping differences are exact)
-            uint32_t sI = __ldg(Sb + 2 * (size_t)xr), sI2 = __ldg(Qb + 2 * (size_t)xr);
-            if (x > 0) {
-                sI -= __ldg(Sb + 2 * (size_t)xlft);
-                sI2 -= __ldg(Qb + 2 * (size_t)xlft);
+        for (int c0 = 0; c0 * 32 < cols; c0 += 4) {
+            uint32_t v[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int x = tx0 + min(lane + 32 * (c0 + u), cols - 1);
+                const size_t xr = (size_t)(x + p.wT - 1), xl = (size_t)(x > 0 ? x - 1 : 0);
+                v[u][0] = __ldg(Sb + 2 * xr);
+                v[u][1] = __ldg(Qb + 2 * xr);
+                v[u][2] = __ldg(Sb + 2 * xl);
+                v[u][3] = __ldg(Qb + 2 * xl);
+                v[u][4] = __ldg(St + 2 * xr);
+                v[u][5] = __ldg(Qt + 2 * xr);
+                v[u][6] = __ldg(St + 2 * xl);
+                v[u][7] = __ldg(Qt + 2 * xl);
             }
-            if (y > 0) {
-                sI -= __ldg(St + 2 * (size_t)xr);
-                sI2 -= __ldg(Qt + 2 * (size_t)xr);
-                if (x > 0) {
-                    sI += __ldg(St + 2 * (size_t)xlft);
-                    sI2 += __ldg(Qt + 2 * (size_t)xlft);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int xo = lane + 32 * (c0 + u), x = tx0 + xo;
+                if (xo >= cols) continue;
+                if (!NCC_BOUNDS(y + p.hT - 1 < p.H && x + p.wT - 1 < p.W &&
+                                    (size_t)y * p.Ox + x < (size_t)p.Oy * p.Ox, p.status))
+                    continue;
+                const int32_t c = (int32_t)brow[ntt::swz(xo)];
+                // box sums from the low 32 bits of S and Q (below 2^32, so the
+                // wrapping differences are exact)
+                const uint32_t xm = x > 0 ? 0xffffffffu : 0u;
+                const uint32_t sI = v[u][0] - (v[u][2] & xm) - (v[u][4] & ym) + (v[u][6] & xm & ym);
+                const uint32_t sI2 = v[u][1] - (v[u][3] & xm) - (v[u][5] & ym) + (v[u][7] & xm & ym);
+                const uint32_t sumIT = (uint32_t)c + 128u * sI + cT;
+                const size_t oi = (size_t)y * p.Ox + x;
+                if (kMoments) {
+                    p.sumI[oi] = (long long)sI;
+                    p.sumI2[oi] = (long long)sI2;
+                    p.sumIT[oi] = (long long)sumIT;
+                } else {
+                    const long long numi =
+                        (long long)((unsigned long long)N * sumIT) - (long long)sI * (long long)sT;
+                    const long long vI =
+                        (long long)((unsigned long long)N * sI2) - (long long)sI * (long long)sI;
+                    const float num = i64_to_f32(numi);
+                    const float vIf = u64_to_f32((unsigned long long)max(vI, 1ll));
+                    // a zero-variance window has num = 0 exactly; invSqrtVT is
+                    // 0 for a zero-variance template
+                    const float r = num * rsqrt_approx(vIf) * invSqrtVT;
+                    __stcs(p.out + oi, fminf(1.0f, fmaxf(-1.0f, r)));
                 }
-            }
-            const uint32_t sumIT = (uint32_t)c + 128u * sI + cT;
-            const size_t oi = (size_t)y * p.Ox + x;
-            if (kMoments) {
-                p.sumI[oi] = (long long)sI;
-                p.sumI2[oi] = (long long)sI2;
-                p.sumIT[oi] = (long long)sumIT;
-            } else {
-                const long long numi = (long long)((unsigned long long)N * sumIT) - (long long)sI * (long long)sT;
-                const long long vI = (long long)((unsigned long long)N * sI2) - (long long)sI * (long long)sI;
-                const float num = i64_to_f32(numi);
-                const float vIf = u64_to_f32((unsigned long long)max(vI, 1ll));
-                // a zero-variance window has num = 0 exactly; invSqrtVT is 0
-                // for a zero-variance template
-                const float rr2 = num * rsqrt_approx(vIf) * invSqrtVT;
-                __stcs(p.out + oi, fminf(1.0f, fmaxf(-1.0f, rr2)));
             }
         }
     }
