@@ -64,6 +64,23 @@ def load_peaks() -> dict:
 # roofline is this times 152 SMs times the maximum SM clock.
 DP4A_PER_SM_CLK = 64
 N_SMS = 152
+# Transform numerator: radix-2 modular butterflies per 256 x 256 tile (two
+# halves of 128 rows; forward and inverse; 256-point row transforms on 128
+# rows, 128-point column transforms on 256 columns).  Its ALU roofline is
+# the SM's instruction issue rate (4 schedulers x 32 lanes per clock) at 7
+# instructions per butterfly (the kernel's butterfly with a twiddle factor:
+# three additions and a minimum on one output, an addition and a Shoup
+# multiplication -- one high and two low products -- on the other).
+NTT_BUTTERFLIES_PER_TILE = 2 * 2 * (128 * 128 * 8 + 256 * 64 * 7)
+NTT_LANE_INSTR_PER_SM_CLK = 128
+NTT_INSTR_PER_BUTTERFLY = 7
+
+
+def ntt_tiles(W: int, H: int, wT: int, hT: int) -> int:
+    """Tiles of the transform numerator (257 - hT rows by (257 - wT) rounded
+    down to 16 columns of shifts each)."""
+    vx, vy = (257 - wT) & ~15, 257 - hT
+    return -(-(W - wT + 1) // vx) * -(-(H - hT + 1) // vy)
 
 # DRAM bytes (read + write) of one launch, from one ncu capture of the bench
 # command (dram__bytes_read.sum + dram__bytes_write.sum; summaries under
@@ -77,6 +94,7 @@ NCU_TRAFFIC_BYTES = {
     ("bank_tc", "bank_2048_64x16"): 1075.6e6,
     ("corr_dp4a_direct", "ncc_4096_t16"): 26.3e6,
     ("corr_toeplitz_tc", "large_8192_t64"): 1476.9e6,
+    ("corr_ntt", "large_8192_t64"): 1444.8e6,
 }
 
 
@@ -460,6 +478,17 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
             r2 = {"kernel": "corr_toeplitz_tc", "workload": w.name, "bound": "tensor",
                   "achieved": tflops, "peak": peak_tc, "unit": "TFLOP/s", "frac": tflops / peak_tc,
                   "traffic": NCU_TRAFFIC_BYTES.get(("corr_toeplitz_tc", w.name))}
+        elif nT == 1 and path == ncc.NCC_PATH_NTT:
+            # modular butterflies (the spectrum kernel's share is in corr_ms
+            # too) against the instruction-issue roofline
+            corr_bytes = CORR_BYTES_PER_COEFF * w.Ox * w.Oy
+            bfly = ntt_tiles(w.W, w.H, w.wT, w.hT) * NTT_BUTTERFLIES_PER_TILE
+            peak_b = (NTT_LANE_INSTR_PER_SM_CLK * N_SMS * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 /
+                      NTT_INSTR_PER_BUTTERFLY)
+            r2 = {"kernel": "corr_ntt", "workload": w.name, "bound": "alu",
+                  "achieved": bfly / (corr_ms * 1e-3) / 1e12, "peak": peak_b / 1e12,
+                  "unit": "Tbutterfly/s", "frac": bfly / (corr_ms * 1e-3) / peak_b,
+                  "traffic": NCU_TRAFFIC_BYTES.get(("corr_ntt", w.name))}
         elif nT == 1:
             # S and Q corners (16 B after reuse) + 1 B image + 4 B out per coefficient
             corr_bytes = CORR_BYTES_PER_COEFF * w.Ox * w.Oy
@@ -505,7 +534,7 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
     metric = METRIC if w.name == DEFAULT_WORKLOAD else f"NCC coefficients/s ({w.name})"
     calls = ("ncc_sat_build + " + ("ncc_correlate" if nT == 1 else
                                    "ncc_correlate_bank" if nT else "nothing"))
-    launches_per_image = (1 if nT else 0) + (1 if variant == 0 else 2)
+    launches_per_image = ((2 if path == ncc.NCC_PATH_NTT else 1) if nT else 0) + (1 if variant == 0 else 2)
     return {
         "metric": metric, "value": value, "unit": UNIT if nT else "pixels/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -527,6 +556,8 @@ def run_gpu(args, w: inputs.Workload) -> dict | None:
         "sat_build": {"ms": sat_ms, "GB/s": sat_gbs, "frac_of_hbm": sat_gbs / hbm},
         "sat_build_8192": sat_large,
         "correlate": corr,
+        "correlate_path": {ncc.NCC_PATH_DP4A: "dp4a", ncc.NCC_PATH_TOEPLITZ: "toeplitz_tc",
+                           ncc.NCC_PATH_NTT: "ntt", ncc.NCC_PATH_BANK: "bank_tc"}.get(path),
         "roofline": {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")},
         "rooflines": rooflines,
         "cpu_baseline": cpu,

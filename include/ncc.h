@@ -149,10 +149,11 @@ int ncc_sat_build_noalloc(const uint8_t *img, int W, int H, int64_t *S,
  * (tcgen05) that writes the sums over 64 consecutive shifts as one matrix
  * product with a Toeplitz factor, from exact centered f16 operands (pixel and
  * template value minus 128) accumulated in fp32 groups of at most 1024
- * products; for wider templates (up to 224 x 224 and 30000 pixels) past the
- * same dp4a count, a numerator from number-theoretic transforms of 256 x 256
- * image tiles (section 15.8's FFT numerator, computed modulo the prime
- * 998244353, which makes it exact; centered values as above), which
+ * products; past the same dp4a count, for templates up to 224 x 224 and
+ * 30000 pixels that are wider than 65 or whose image gives at least 3.5
+ * tiles per multiprocessor, a numerator from number-theoretic transforms of
+ * 256 x 256 image tiles (section 15.8's FFT numerator, computed modulo the
+ * prime 998244353, which makes it exact; centered values as above), which
  * allocates the template's 512 KB spectrum from the library's stream-ordered
  * pool for the duration of the call.  All produce the same integer sums and
  * the same coefficients.

@@ -45,9 +45,15 @@ constexpr int kMaxW = 66051;  // 66051 * 255^2 < 2^32: a row's running sum of sq
 // with it; they cross between 32x32 (256 per output: dp4a faster at every
 // image size tried) and 40x40 (400: the Toeplitz kernel faster).
 constexpr long long kToeplitzMinDp4a = 320;
-// Templates too wide for the Toeplitz kernel go to the transform kernel
-// from the same dp4a count on.
+// Past the same dp4a count the transform kernel takes templates too wide for
+// the Toeplitz kernel, and the others too once the image gives it at least
+// 3.5 tiles per SM: measured on this GPU (one call each, 40x40 to 64x64
+// templates on 2048^2 to 8192^2 images), it is as fast as or slower than
+// the Toeplitz kernel below about three rounds of tiles (4096^2, 64x64: 463
+// against 423 us) and faster from four on (5120^2, 40x40: 521 against
+// 587 us; 8192^2, 64x64: 1390 against 1751 us).
 constexpr long long kNttMinDp4a = 320;
+constexpr long long kNttMinTilesPerSm2 = 7;  // tiles >= 3.5 x SMs
 constexpr long long kMaxN = 66051;  // wT*hT*255^2 < 2^32: SumIT fits uint32
 
 int status_ptr(int **out) {
@@ -160,9 +166,10 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
         return rc;
     }
     if (direct) path = NCC_PATH_DP4A;  // the direct moments exist on the dp4a kernel only
-    // The single-template kernel: forced, or automatically the Toeplitz
-    // tensor-core product for wide templates, whose numerator dominates, the
-    // transform kernel for templates wider than that, dp4a otherwise.
+    // The single-template kernel: forced, or automatically (for templates
+    // whose numerator dominates) the transform kernel on large images and
+    // for templates too wide for the Toeplitz tensor-core product, that
+    // product otherwise, and dp4a for smaller templates.
     const long long dp4aPerOutput = (long long)((wT + 3) / 4) * hT;
     int kernel = NCC_PATH_DP4A;
     if (path == NCC_PATH_TOEPLITZ || path == NCC_PATH_NTT) {
@@ -171,10 +178,12 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
         if (!ok) return NCC_ERR_UNSUPPORTED;
         kernel = path;
     } else if (path == 0) {
-        if (ncc::corr_toeplitz_supported(wT, hT) && dp4aPerOutput >= kToeplitzMinDp4a)
-            kernel = NCC_PATH_TOEPLITZ;
-        else if (ncc::corr_ntt_supported(wT, hT) && dp4aPerOutput >= kNttMinDp4a)
+        const bool tz = ncc::corr_toeplitz_supported(wT, hT) && dp4aPerOutput >= kToeplitzMinDp4a;
+        const bool nt = ncc::corr_ntt_supported(wT, hT) && dp4aPerOutput >= kNttMinDp4a;
+        if (nt && (!tz || 2 * ncc::corr_ntt_tiles(W, H, wT, hT) >= kNttMinTilesPerSm2 * ncc::sm_count()))
             kernel = NCC_PATH_NTT;
+        else if (tz)
+            kernel = NCC_PATH_TOEPLITZ;
     }
     if (kernel == NCC_PATH_DP4A && !ncc::corr_dp4a_supported(wT, hT)) return NCC_ERR_UNSUPPORTED;
     int used = NCC_PATH_NONE;

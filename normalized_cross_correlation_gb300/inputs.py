@@ -141,6 +141,16 @@ def large_8192(seed: int = 4) -> Workload:
     return Workload("large_8192_t64", img, T, [(0, 4000, 6000)])
 
 
+def wide_4096(seed: int = 5) -> Workload:
+    """4096x4096 3x3-box-blurred noise; template = 128x128 crop at
+    (1500, 2500): wider than the Toeplitz tensor-core kernel takes, so the
+    transform numerator serves it (about 4096 dp4a per output otherwise)."""
+    rng = np.random.default_rng(seed)
+    img = box_blurred_image(rng, 4096, 4096, 3)
+    T = crop(img, 1500, 2500, 128, 128)[None]
+    return Workload("wide_4096_t128", img, T, [(0, 1500, 2500)])
+
+
 def sat_8192(seed: int = 4) -> Workload:
     """The 8192x8192 image of :func:`large_8192`, tables only (no template)."""
     return Workload("sat_8192", large_8192(seed).image, None, [])
@@ -153,6 +163,7 @@ NAMED = {
     "ncc_4096_t16": headline_4096,
     "bank_2048_64x16": bank_2048,
     "large_8192_t64": large_8192,
+    "wide_4096_t128": wide_4096,
     "sat_8192": sat_8192,
 }
 

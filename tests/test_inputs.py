@@ -59,6 +59,16 @@ def test_large_workload():
     assert abs(lo - 0.1) < 0.005 and abs(hi - 0.1) < 0.005
 
 
+def test_wide_workload():
+    """The transform numerator's workload: a 3x3 box blur of uniform noise
+    (values spread around 128, none saturated) with a 128x128 crop."""
+    w = inputs.wide_4096()
+    assert w.image.shape == (4096, 4096) and w.templates.shape == (1, 128, 128)
+    np.testing.assert_array_equal(w.templates[0], w.image[2500:2628, 1500:1628])
+    assert abs(float(w.image.mean()) - 127.5) < 0.5
+    assert abs(float(w.image.std()) - 73.9 / 3) < 0.5   # a 3x3 mean of uniform bytes
+
+
 def test_generators_are_deterministic():
     a, b = inputs.random_case(7, 300, 200, 9, 5, nT=3, n_crops=2), \
         inputs.random_case(7, 300, 200, 9, 5, nT=3, n_crops=2)
