@@ -332,9 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1) ntt_corr_kernel(const NttParams p
             uint32_t *row = t.buf + r * ntt::kStride;
 #pragma unroll
             for (int a = 0; a < 16; ++a) {
-                const uint32_t ov = ntt::mulw(o[a], rf);
-                row[16 * a + (n2 ^ a)] = (uint32_t)ntt::centered(e[a] + ov);
-                e[a] = (uint32_t)ntt::centered(e[a] - ov + kP2);
+                const uint32_t ov = ntt::mulw(o[a], rf), ev = ntt::red2(e[a]);  // both in [0, 2p)
+                row[16 * a + (n2 ^ a)] = (uint32_t)ntt::centered(ev + ov);
+                e[a] = (uint32_t)ntt::centered(ev - ov + kP2);
             }
             tm_st16(tm + 16 * k, e);
         }

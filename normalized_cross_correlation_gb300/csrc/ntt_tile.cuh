@@ -137,7 +137,10 @@ __host__ __device__ __forceinline__ void dif(uint32_t (&v)[N]) {
 }
 
 // The inverse (unnormalized: N times the inverse transform), decimation in
-// time: bit-reversed order in, natural order out.
+// time: bit-reversed order in, natural order out.  Inputs and outputs in
+// [0, 4p): a butterfly reduces its first input to [0, 2p), multiplies the
+// second (any 32-bit value) to [0, 2p), and leaves the sum and the
+// difference + 2p unreduced.
 template <int N>
 __host__ __device__ __forceinline__ void dit_inv(uint32_t (&v)[N]) {
     static_assert(N == 8 || N == 16, "8 or 16 points");
@@ -148,11 +151,14 @@ __host__ __device__ __forceinline__ void dit_inv(uint32_t (&v)[N]) {
                 constexpr int j = decltype(J)::value;
                 constexpr int a = decltype(Bk)::value * 2 * h + j, b = a + h;
                 constexpr uint32_t w = pow_c(kW16Inv, (uint32_t)(j * (8 / h)));  // w_(2h)^-j
-                const uint32_t u = v[a];
-                uint32_t t = v[b];
-                if constexpr (j != 0) t = mulw(t, w, shoup_c(w));
-                v[a] = red2(u + t);
-                v[b] = red2(u - t + kP2);
+                const uint32_t u = red2(v[a]);
+                uint32_t t;
+                if constexpr (j == 0)
+                    t = red2(v[b]);
+                else
+                    t = mulw(v[b], w, shoup_c(w));
+                v[a] = u + t;
+                v[b] = u - t + kP2;
             });
         });
     });
@@ -236,7 +242,8 @@ __host__ __device__ __forceinline__ void rows_fwd1(int tid, const Tile &t, Load 
     }
 }
 
-// (2) rows, second radix-16 pass (16 consecutive columns)
+// (2) rows, second radix-16 pass (16 consecutive columns).  The forward
+// passes keep values in [0, 2p); the inverse passes take [0, 4p).
 __host__ __device__ __forceinline__ void rows_fwd2(int tid, const Tile &t) {
 #pragma unroll 1
     for (int k = 0; k < 4; ++k) {
@@ -353,7 +360,7 @@ __host__ __device__ __forceinline__ void rows_inv1(int tid, const Tile &t) {
 }
 
 // (7) rows, last inverse pass for item k of this thread (row r = idx/16,
-// columns 16a + idx%16): out[a] in [0, 2p), natural order
+// columns 16a + idx%16): out[a] in [0, 4p), natural order
 __host__ __device__ __forceinline__ void rows_inv2(int tid, int k, const Tile &t, uint32_t (&out)[16]) {
     const int idx = tid + kThreads * k, r = idx >> 4, n2 = idx & 15;
     const uint32_t *row = t.buf + r * kStride;
@@ -365,7 +372,9 @@ __host__ __device__ __forceinline__ void rows_inv2(int tid, int k, const Tile &t
     dit_inv<16>(out);
 }
 
-// Centered integer from a residue in [0, 4p) of a value |C| < p/2.
+// Centered integer from a residue in [0, 4p) of a value |C| < p/2.  (The
+// inverse passes leave values in [0, 4p); products by a factor are in
+// [0, 2p); a sum of the two needs its first term reduced first.)
 __host__ __device__ __forceinline__ int32_t centered(uint32_t s) {
     s = red1(red2(s));
     return s > (kP >> 1) ? (int32_t)(s - kP) : (int32_t)s;
