@@ -24,7 +24,8 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 SUITES = ["tests/test_sat_gpu.py", "tests/test_correlate_gpu.py",
-          "tests/test_correlate_toeplitz_gpu.py", "tests/test_bank_gpu.py",
+          "tests/test_correlate_toeplitz_gpu.py", "tests/test_correlate_ntt_gpu.py",
+          "tests/test_bank_gpu.py",
           "tests/test_direct_gpu.py", "tests/test_match_gpu.py",
           "tests/test_sat_ladder_gpu.py"]
 
