@@ -255,7 +255,9 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     const Geom &g = p.g;
     const int epiBW = kNarrow ? kNarrowBW : g.epiBW, epiBuf = kNarrow ? kNarrowBuf : g.epiBuf;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int x0 = blockIdx.x * kOutW, y0 = blockIdx.y * kTileH;
+    // tile rows bottom-up: the table build writes its tables top-down, so
+    // the last rows it wrote -- still in L2 -- are read first
+    const int x0 = blockIdx.x * kOutW, y0 = (gridDim.y - 1 - blockIdx.y) * kTileH;
     const int epiSteps = (min(kTileH, p.Oy - y0) + kEpiRowsPerStep - 1) / kEpiRowsPerStep;
     uint8_t *epi = smem + g.epiOff;
     // table-row segments of epilogue step t: rows y0+2t+h, buffers
