@@ -92,7 +92,7 @@ NCU_TRAFFIC_BYTES = {
     ("sat_build", "sat_8192"): 1107.0e6,
     ("corr_dp4a", "ncc_4096_t16"): 337.7e6,
     ("bank_tc", "bank_2048_64x16"): 1075.6e6,
-    ("corr_dp4a_direct", "ncc_4096_t16"): 26.3e6,
+    ("corr_dp4a_direct", "ncc_4096_t16"): 25.6e6,
     ("corr_toeplitz_tc", "large_8192_t64"): 1476.9e6,
     ("corr_ntt", "large_8192_t64"): 1444.8e6,
 }
