@@ -143,20 +143,20 @@ int ncc_sat_build_noalloc(const uint8_t *img, int W, int H, int64_t *S,
  *   S, Q device int64 [H][W]: must hold ncc_sat_build(img) output, ordered
  *        before this call (same stream, or an event).
  *   out  device fp32 [Oy][Ox], written completely; must not overlap inputs.
- * Kernels: the integer dot-product (dp4a) numerator, or -- for templates up
- * to 65 pixels wide whose dp4a numerator would take at least 320 dp4a per
- * output, ceil(wT/4)*hT (about 40x40 and up) -- a tensor-core numerator
- * (tcgen05) that writes the sums over 64 consecutive shifts as one matrix
- * product with a Toeplitz factor, from exact centered f16 operands (pixel and
- * template value minus 128) accumulated in fp32 groups of at most 1024
- * products; past the same dp4a count, for templates up to 224 x 224 and
- * 30000 pixels that are wider than 65 or whose image gives at least 3.5
- * tiles per multiprocessor, a numerator from number-theoretic transforms of
- * 256 x 256 image tiles (section 15.8's FFT numerator, computed modulo the
- * prime 998244353, which makes it exact; centered values as above), which
- * allocates the template's 512 KB spectrum from the library's stream-ordered
- * pool for the duration of the call.  All produce the same integer sums and
- * the same coefficients.
+ * Kernels: the integer dot-product (dp4a) numerator; for templates up to 65
+ * pixels wide whose dp4a numerator would take at least 96 dp4a per output,
+ * ceil(wT/4)*hT (about 20x20 and up; 320, about 40x40, on maps of fewer than
+ * 4M shifts), a tensor-core numerator (tcgen05) that writes the sums over 64
+ * consecutive shifts as one matrix product with a Toeplitz factor, from exact
+ * centered f16 operands (pixel and template value minus 128) accumulated in
+ * fp32 groups of at most 1024 products; for templates that kernel cannot
+ * take (wider than 65, or too tall for its accumulator groups) up to
+ * 224 x 224 and 30000 pixels, from 320 dp4a per output, a numerator from
+ * number-theoretic transforms of 256 x 256 image tiles (section 15.8's FFT
+ * numerator, computed modulo the prime 998244353, which makes it exact;
+ * centered values as above), which allocates the template's 512 KB spectrum
+ * from the library's stream-ordered pool for the duration of the call.  All
+ * produce the same integer sums and the same coefficients.
  * Returns NCC_OK, NCC_ERR_INVALID_ARG, NCC_ERR_UNSUPPORTED, NCC_ERR_NOMEM
  * (the spectrum could not be allocated) or NCC_ERR_CUDA.
  */

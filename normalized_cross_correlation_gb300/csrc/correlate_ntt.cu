@@ -366,12 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1) ntt_corr_kernel(const NttParams p
 
 }  // namespace
 
-long long corr_ntt_tiles(int W, int H, int wT, int hT) {
-    const long long Vx = (kL + 1 - wT) & ~15, Vy = kL + 1 - hT;
-    const long long Ox = W - wT + 1, Oy = H - hT + 1;
-    return ((Ox + Vx - 1) / Vx) * ((Oy + Vy - 1) / Vy);
-}
-
 bool corr_ntt_supported(int wT, int hT) {
     return wT >= 1 && hT >= 1 && wT <= kMaxSide && hT <= kMaxSide &&
            (long long)wT * hT <= ntt::kMaxPixels;

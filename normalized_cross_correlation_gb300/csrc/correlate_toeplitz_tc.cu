@@ -565,47 +565,66 @@ __global__ void __launch_bounds__(kThreads, 1) toeplitz_tc_kernel(const TParams 
             if (lane == 0) mbar_arrive(&accEmpty[ab]);
             // (2) one output row at a time, lane = shift: coalesced box sums
             // from the low 32 bits of S and Q (the box sums are below 2^32,
-            // so wrapping differences are exact) and coalesced stores
+            // so wrapping differences are exact) and coalesced stores.  The
+            // table reads of four rows are issued before any is used; their
+            // addresses are clamped into the tables (x to the last shift, the
+            // rows above row 0 to row 0, masked out), so every read is in
+            // bounds and only the stores are conditional.
             const int x = x0 + 32 * hf + lane;
-            const int xl = x - 1, xr = x + p.wT - 1;
             const bool xin = x < p.Ox;
+            const int xc = min(x, p.Ox - 1);
+            const size_t xr2 = 2 * (size_t)(xc + p.wT - 1), xl2 = 2 * (size_t)(xc > 0 ? xc - 1 : 0);
+            const uint32_t xm = xc > 0 ? 0xffffffffu : 0u;
             const int rows = min(32, p.Oy - (y0 + 32 * qd));
-#pragma unroll 4
-            for (int r = 0; r < rows; ++r) {
-                const int y = y0 + 32 * qd + r;
-                const int c = X[r * 33 + lane];
-                if (!xin) continue;
-                if (!NCC_BOUNDS(y + p.hT - 1 < p.H && xr < p.W && (size_t)y * p.Ox + x <
-                                    (size_t)p.Oy * p.Ox, p.status))
-                    continue;
-                const unsigned *Sb = reinterpret_cast<const unsigned *>(p.S + (size_t)(y + p.hT - 1) * W);
-                const unsigned *Qb = reinterpret_cast<const unsigned *>(p.Q + (size_t)(y + p.hT - 1) * W);
-                uint32_t sI = __ldg(Sb + 2 * (size_t)xr), sI2 = __ldg(Qb + 2 * (size_t)xr);
-                if (x > 0) { sI -= __ldg(Sb + 2 * (size_t)xl); sI2 -= __ldg(Qb + 2 * (size_t)xl); }
-                if (y > 0) {
-                    const unsigned *St = reinterpret_cast<const unsigned *>(p.S + (size_t)(y - 1) * W);
-                    const unsigned *Qt = reinterpret_cast<const unsigned *>(p.Q + (size_t)(y - 1) * W);
-                    sI -= __ldg(St + 2 * (size_t)xr);
-                    sI2 -= __ldg(Qt + 2 * (size_t)xr);
-                    if (x > 0) { sI += __ldg(St + 2 * (size_t)xl); sI2 += __ldg(Qt + 2 * (size_t)xl); }
+            for (int r0 = 0; r0 < rows; r0 += 4) {
+                uint32_t v[4][8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int y = y0 + 32 * qd + min(r0 + u, rows - 1);
+                    const unsigned *Sb = reinterpret_cast<const unsigned *>(p.S + (size_t)(y + p.hT - 1) * W);
+                    const unsigned *Qb = reinterpret_cast<const unsigned *>(p.Q + (size_t)(y + p.hT - 1) * W);
+                    const unsigned *St = reinterpret_cast<const unsigned *>(p.S + (size_t)(y > 0 ? y - 1 : 0) * W);
+                    const unsigned *Qt = reinterpret_cast<const unsigned *>(p.Q + (size_t)(y > 0 ? y - 1 : 0) * W);
+                    v[u][0] = __ldg(Sb + xr2);
+                    v[u][1] = __ldg(Qb + xr2);
+                    v[u][2] = __ldg(Sb + xl2);
+                    v[u][3] = __ldg(Qb + xl2);
+                    v[u][4] = __ldg(St + xr2);
+                    v[u][5] = __ldg(Qt + xr2);
+                    v[u][6] = __ldg(St + xl2);
+                    v[u][7] = __ldg(Qt + xl2);
                 }
-                const uint32_t sumIT = (uint32_t)c + 128u * sI + cT;
-                const size_t o = (size_t)y * p.Ox + x;
-                if (kMoments) {
-                    p.sumI[o] = (long long)sI;
-                    p.sumI2[o] = (long long)sI2;
-                    p.sumIT[o] = (long long)sumIT;
-                } else {
-                    const long long numi = (long long)((unsigned long long)N * sumIT) -
-                                           (long long)sI * (long long)sT;
-                    const long long vI = (long long)((unsigned long long)N * sI2) -
-                                         (long long)sI * (long long)sI;
-                    const float num = i64_to_f32(numi);
-                    const float vIf = u64_to_f32((unsigned long long)max(vI, 1ll));
-                    // a zero-variance window has num = 0 exactly; invSqrtVT is 0
-                    // for a zero-variance template
-                    const float rr = num * rsqrt_approx(vIf) * invSqrtVT;
-                    __stcs(p.out + o, fminf(1.0f, fmaxf(-1.0f, rr)));
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int r = r0 + u;
+                    if (r >= rows) break;
+                    const int y = y0 + 32 * qd + r;
+                    const int c = X[r * 33 + lane];
+                    if (!xin) continue;
+                    if (!NCC_BOUNDS(y + p.hT - 1 < p.H && x + p.wT - 1 < p.W && (size_t)y * p.Ox + x <
+                                        (size_t)p.Oy * p.Ox, p.status))
+                        continue;
+                    const uint32_t ym = y > 0 ? 0xffffffffu : 0u;
+                    const uint32_t sI = v[u][0] - (v[u][2] & xm) - (v[u][4] & ym) + (v[u][6] & xm & ym);
+                    const uint32_t sI2 = v[u][1] - (v[u][3] & xm) - (v[u][5] & ym) + (v[u][7] & xm & ym);
+                    const uint32_t sumIT = (uint32_t)c + 128u * sI + cT;
+                    const size_t o = (size_t)y * p.Ox + x;
+                    if (kMoments) {
+                        p.sumI[o] = (long long)sI;
+                        p.sumI2[o] = (long long)sI2;
+                        p.sumIT[o] = (long long)sumIT;
+                    } else {
+                        const long long numi = (long long)((unsigned long long)N * sumIT) -
+                                               (long long)sI * (long long)sT;
+                        const long long vI = (long long)((unsigned long long)N * sI2) -
+                                             (long long)sI * (long long)sI;
+                        const float num = i64_to_f32(numi);
+                        const float vIf = u64_to_f32((unsigned long long)max(vI, 1ll));
+                        // a zero-variance window has num = 0 exactly; invSqrtVT is
+                        // 0 for a zero-variance template
+                        const float rr = num * rsqrt_approx(vIf) * invSqrtVT;
+                        __stcs(p.out + o, fminf(1.0f, fmaxf(-1.0f, rr)));
+                    }
                 }
             }
             __syncwarp();  // the block is read before the next tile overwrites it

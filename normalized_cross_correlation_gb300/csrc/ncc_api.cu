@@ -38,22 +38,24 @@ void set_last_path(int path) {
 }
 
 constexpr int kMaxW = 66051;  // 66051 * 255^2 < 2^32: a row's running sum of squares fits uint32
-// Automatic selection gives a single template to the Toeplitz kernel when
-// the dp4a numerator would take at least this many dp4a per output
-// (ceil(wT/4) * hT).  Measured on this GPU, the Toeplitz kernel's time hardly
-// depends on the template (its box-sum epilogue binds) while dp4a's grows
-// with it; they cross between 32x32 (256 per output: dp4a faster at every
-// image size tried) and 40x40 (400: the Toeplitz kernel faster).
-constexpr long long kToeplitzMinDp4a = 320;
-// Past the same dp4a count the transform kernel takes templates too wide for
-// the Toeplitz kernel, and the others too once the image gives it at least
-// 3.5 tiles per SM: measured on this GPU (one call each, 40x40 to 64x64
-// templates on 2048^2 to 8192^2 images), it is as fast as or slower than
-// the Toeplitz kernel below about three rounds of tiles (4096^2, 64x64: 463
-// against 423 us) and faster from four on (5120^2, 40x40: 521 against
-// 587 us; 8192^2, 64x64: 1390 against 1751 us).
+// Automatic selection of the single-template numerator, from a sweep of all
+// three kernels on this GPU (one call each, 16x16 to 64x64 templates on
+// 1024^2 to 8192^2 images):
+//   - the Toeplitz tensor-core kernel's time hardly depends on the template
+//     (its box-sum epilogue binds), dp4a's grows with ceil(wT/4)*hT; on maps
+//     of at least 4M shifts they cross between 16x16 (64 dp4a per output:
+//     4096^2 dp4a 100 us, Toeplitz 181 us) and 20x20 (100: 212 against
+//     188 us);
+//   - on smaller maps they tie up to 32x32 (1024^2: 33 us each), where dp4a
+//     keeps the templates below 320 dp4a per output, since inside ncc_match
+//     only it overlaps the table build;
+//   - the transform kernel is slower than the Toeplitz kernel for every
+//     template the latter takes (8192^2, 64x64: 1316 against 1224 us), and
+//     takes the wider ones from 320 dp4a per output on.
+constexpr long long kToeplitzMinDp4a = 96;
+constexpr long long kToeplitzMinOutputs = 4000000;
+constexpr long long kToeplitzMinDp4aSmall = 320;
 constexpr long long kNttMinDp4a = 320;
-constexpr long long kNttMinTilesPerSm2 = 7;  // tiles >= 3.5 x SMs
 constexpr long long kMaxN = 66051;  // wT*hT*255^2 < 2^32: SumIT fits uint32
 
 int status_ptr(int **out) {
@@ -167,9 +169,9 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
     }
     if (direct) path = NCC_PATH_DP4A;  // the direct moments exist on the dp4a kernel only
     // The single-template kernel: forced, or automatically (for templates
-    // whose numerator dominates) the transform kernel on large images and
-    // for templates too wide for the Toeplitz tensor-core product, that
-    // product otherwise, and dp4a for smaller templates.
+    // whose numerator dominates) the Toeplitz tensor-core product, the
+    // transform kernel for templates that product cannot take, and dp4a
+    // for smaller templates.
     const long long dp4aPerOutput = (long long)((wT + 3) / 4) * hT;
     int kernel = NCC_PATH_DP4A;
     if (path == NCC_PATH_TOEPLITZ || path == NCC_PATH_NTT) {
@@ -178,12 +180,12 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
         if (!ok) return NCC_ERR_UNSUPPORTED;
         kernel = path;
     } else if (path == 0) {
-        const bool tz = ncc::corr_toeplitz_supported(wT, hT) && dp4aPerOutput >= kToeplitzMinDp4a;
-        const bool nt = ncc::corr_ntt_supported(wT, hT) && dp4aPerOutput >= kNttMinDp4a;
-        if (nt && (!tz || 2 * ncc::corr_ntt_tiles(W, H, wT, hT) >= kNttMinTilesPerSm2 * ncc::sm_count()))
-            kernel = NCC_PATH_NTT;
-        else if (tz)
+        const bool tzOk = ncc::corr_toeplitz_supported(wT, hT);
+        const long long tzMin = (long long)plane >= kToeplitzMinOutputs ? kToeplitzMinDp4a : kToeplitzMinDp4aSmall;
+        if (tzOk && dp4aPerOutput >= tzMin)
             kernel = NCC_PATH_TOEPLITZ;
+        else if (!tzOk && ncc::corr_ntt_supported(wT, hT) && dp4aPerOutput >= kNttMinDp4a)
+            kernel = NCC_PATH_NTT;
     }
     if (kernel == NCC_PATH_DP4A && !ncc::corr_dp4a_supported(wT, hT)) return NCC_ERR_UNSUPPORTED;
     int used = NCC_PATH_NONE;

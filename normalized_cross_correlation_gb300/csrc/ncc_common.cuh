@@ -196,8 +196,6 @@ cudaError_t corr_toeplitz_launch(const CorrArgs &a, cudaStream_t stream);
 // (512 KB) from the library's stream-ordered pool for the duration of the
 // call.
 bool corr_ntt_supported(int wT, int hT);
-// Its 256 x 256 tiles for a W x H image (one CTA per SM takes them in turn).
-long long corr_ntt_tiles(int W, int H, int wT, int hT);
 cudaError_t corr_ntt_launch(const CorrArgs &a, cudaStream_t stream);
 
 // Template-bank correlation on the tensor cores (tcgen05, f16 operands,

@@ -82,7 +82,7 @@ def test_bank_2048_64x16(ncc, threads):
 def test_large_8192_t64(ncc, threads):
     r = check_workload(ncc, threads, inputs.large_8192())
     assert r.shape == (1, 8129, 8129)
-    assert ncc.ncc_debug_last_path() == ncc.NCC_PATH_NTT   # 1849 tiles: the transform kernel
+    assert ncc.ncc_debug_last_path() == ncc.NCC_PATH_TOEPLITZ
 
 
 def test_wide_4096_t128(ncc, threads):

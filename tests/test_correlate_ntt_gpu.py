@@ -158,16 +158,18 @@ def test_automatic_selection_takes_ntt_for_wide_templates(ncc):
     assert ncc.ncc_sync_status() == 0
 
 
-def test_automatic_selection_by_image_size(ncc):
-    """For templates both tensor-core-era kernels take, the transform kernel
-    runs once the image gives it at least 3.5 tiles per SM."""
-    small = to_dev(np.zeros((1500, 1500), np.uint8))
-    large = to_dev(np.zeros((6000, 6000), np.uint8))      # 31 x 31 tiles at 64 x 64
-    T = to_dev(np.random.default_rng(3).integers(0, 256, (64, 64), dtype=np.uint8))
-    for img, path in ((small, ncc.NCC_PATH_TOEPLITZ), (large, ncc.NCC_PATH_NTT)):
-        S, Q = ncc.ncc_sat_build(img)
-        ncc.ncc_correlate(img, T, S, Q)
-        assert ncc.ncc_debug_last_path() == path
+def test_automatic_selection_at_every_image_size(ncc):
+    """Templates the Toeplitz kernel takes stay on it on large images too;
+    the transform kernel takes the wider ones and those too tall for the
+    Toeplitz kernel's accumulator groups (40 x 200: eight groups of 25 rows)."""
+    large = to_dev(np.zeros((6000, 6000), np.uint8))
+    rng = np.random.default_rng(3)
+    for shape, path in (((64, 64), ncc.NCC_PATH_TOEPLITZ), ((80, 80), ncc.NCC_PATH_NTT),
+                        ((200, 40), ncc.NCC_PATH_NTT)):
+        T = to_dev(rng.integers(0, 256, shape, dtype=np.uint8))
+        S, Q = ncc.ncc_sat_build(large)
+        ncc.ncc_correlate(large, T, S, Q)
+        assert ncc.ncc_debug_last_path() == path, shape
         del S, Q
     assert ncc.ncc_sync_status() == 0
 

@@ -119,8 +119,9 @@ def test_toeplitz_zero_variance_and_negated_crop(toeplitz):
 
 
 def test_automatic_selection_takes_toeplitz_for_large_templates(ncc):
-    """Toeplitz from ceil(wT/4)*hT >= 320 dp4a per output (40x40 and up),
-    dp4a below (32x32, and wide but short templates)."""
+    """On maps of fewer than 4M shifts: Toeplitz from ceil(wT/4)*hT >= 320
+    dp4a per output (40x40 and up), dp4a below (32x32, and wide but short
+    templates)."""
     w = inputs.random_case(5, 300, 200, 64, 64, nT=1, n_crops=1)
     dimg = to_dev(w.image)
     S, Q = ncc.ncc_sat_build(dimg)
@@ -130,6 +131,19 @@ def test_automatic_selection_takes_toeplitz_for_large_templates(ncc):
                        (T[:, :16], ncc.NCC_PATH_DP4A)):
         ncc.ncc_correlate(dimg, to_dev(tmpl), S, Q)
         assert ncc.ncc_debug_last_path() == path, tmpl.shape
+    assert ncc.ncc_sync_status() == 0
+
+
+def test_automatic_selection_on_large_maps(ncc):
+    """On maps of at least 4M shifts: Toeplitz from 96 dp4a per output
+    (20x20: 100), dp4a below (16x16: 64; 64 x 4: 64)."""
+    img = to_dev(np.zeros((2200, 2200), np.uint8))
+    S, Q = ncc.ncc_sat_build(img)
+    rng = np.random.default_rng(8)
+    for shape, path in (((20, 20), ncc.NCC_PATH_TOEPLITZ), ((16, 16), ncc.NCC_PATH_DP4A),
+                        ((4, 64), ncc.NCC_PATH_DP4A), ((24, 16), ncc.NCC_PATH_TOEPLITZ)):
+        ncc.ncc_correlate(img, to_dev(rng.integers(0, 256, shape, dtype=np.uint8)), S, Q)
+        assert ncc.ncc_debug_last_path() == path, shape
     assert ncc.ncc_sync_status() == 0
 
 
