@@ -76,6 +76,31 @@ def test_ntt_coefficients_match_oracle(ntt, threads, W, H, wT, hT):
 
 
 @pytest.mark.parametrize("img_v,tmpl_v", [(0, 0), (255, 0), (0, 255), (255, 255)])
+@pytest.mark.parametrize("img_offset", [0, 3])
+def test_ntt_image_pointer_alignment(ntt, threads, img_offset):
+    """Rows a multiple of 16 bytes long: from a 16-byte-aligned image the
+    tile rows are staged with 16-byte loads, from an image 3 bytes into its
+    buffer byte by byte; both through the C ABI, bit for bit the same."""
+    import torch
+    ncc = ntt
+    w = inputs.random_case(4242, 640, 480, 96, 72, nT=1, n_crops=1)
+    n = w.image.size
+    ibuf = torch.zeros(n + 64, dtype=torch.uint8, device="cuda")
+    ibuf[img_offset:img_offset + n] = torch.from_numpy(w.image.ravel()).cuda()
+    dimg = to_dev(w.image)
+    S, Q = ncc.ncc_sat_build(dimg)
+    out = nan_map(w.Oy, w.Ox)
+    tm = to_dev(w.templates[0])
+    rc = ncc.lib().ncc_correlate(ibuf.data_ptr() + img_offset, w.W, w.H, tm.data_ptr(), w.wT, w.hT,
+                                 S.data_ptr(), Q.data_ptr(), out.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, ncc.ncc_status_string(rc)
+    assert ncc.ncc_sync_status() == 0
+    assert ncc.ncc_debug_last_path() == ncc.NCC_PATH_NTT
+    ref = oracle.correlate(w.image, w.templates[0], threads=threads)
+    np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=0, atol=TOL)
+
+
 def test_ntt_extreme_centered_sums(ntt, threads, img_v, tmpl_v):
     """A constant image block at 0 or 255 against a constant 173 x 173
     template at 0 or 255: every centered product is +-16384 or +-16256, so
