@@ -75,7 +75,6 @@ def test_ntt_coefficients_match_oracle(ntt, threads, W, H, wT, hT):
         assert abs(r[y, x] - 1.0) <= TOL
 
 
-@pytest.mark.parametrize("img_v,tmpl_v", [(0, 0), (255, 0), (0, 255), (255, 255)])
 @pytest.mark.parametrize("img_offset", [0, 3])
 def test_ntt_image_pointer_alignment(ntt, threads, img_offset):
     """Rows a multiple of 16 bytes long: from a 16-byte-aligned image the
@@ -101,6 +100,7 @@ def test_ntt_image_pointer_alignment(ntt, threads, img_offset):
     np.testing.assert_allclose(out.cpu().numpy(), ref, rtol=0, atol=TOL)
 
 
+@pytest.mark.parametrize("img_v,tmpl_v", [(0, 0), (255, 0), (0, 255), (255, 255)])
 def test_ntt_extreme_centered_sums(ntt, threads, img_v, tmpl_v):
     """A constant image block at 0 or 255 against a constant 173 x 173
     template at 0 or 255: every centered product is +-16384 or +-16256, so
