@@ -11,8 +11,9 @@
 // because |C| <= 2^14 * wT * hT < p / 2.
 //
 // The prime is p = 119 * 2^23 + 1 (3 generates its multiplicative group), so
-// 256th roots of unity exist and 4p < 2^32: values stay in [0, 2p) between
-// operations ("lazy" reduction) and sums of two never overflow 32 bits.
+// 256th roots of unity exist and 4p < 2^32: values are reduced only lazily --
+// the forward passes keep them in [0, 2p), the inverse passes in [0, 4p) --
+// and no sum overflows 32 bits.
 // Multiplication by a known factor w uses its precomputed companion
 // wq = floor(w * 2^32 / p) (Shoup's method): q = hi32(x * wq) and
 // x * w - q * p lies in [0, 2p) for any 32-bit x.
