@@ -368,11 +368,6 @@ int ncc_match(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int
         return NCC_ERR_INVALID_ARG;
     rc = ncc_sat_build(img, W, H, S, Q, stream);   // checks S, Q against img and each other
     if (rc != NCC_OK) return rc;
-    int path;
-    {
-        std::lock_guard<std::mutex> lock(g_mutex);
-        path = g_path;
-    }
     // the overlap only behind the fused builder, which lets its dependents start
     return run_correlate(img, W, H, tmpl, wT, hT, nT, S, Q, out, nullptr, nullptr, nullptr,
                          reinterpret_cast<cudaStream_t>(stream), true);
