@@ -568,8 +568,13 @@ __global__ void __launch_bounds__(kThreads, 2) bank_tc_kernel(const BParams p) {
                                      (long long)((int)sI) * (long long)((int)sI);
                 const float rsI = vI > 0 ? rsqrt_approx(u64_to_f32((unsigned long long)vI)) : 0.f;
                 const float sIf = (float)(int)sI;  // < 2^25: exact
-                if (valid) {
+                // wait for the accumulator even for an invalid row: this warp's
+                // aempty arrival below must not land before the stage's
+                // previous use is complete, or it would count toward that use
+                // and let the issuer overwrite the stage while the other warp
+                // of the lane quarter still reads it
                 mbar_wait_warp(&afull[a], ka & 1, &s_abort, p.status);
+                if (valid) {
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const size_t obase = (size_t)y * p.Ox + x;
                 // lanes whose output (or window) a check finds outside the

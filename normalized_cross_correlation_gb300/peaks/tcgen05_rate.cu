@@ -256,6 +256,163 @@ __global__ void rate_kernel(long long *cyc, int nmma, int *err) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tm), "r"(cols));
 }
 
+// The bank kernel's accumulator pattern on its operand layout (N = 128, A
+// MN-major over shifted copies): chains of `chain` MMAs, the first of each
+// overwriting its accumulator, accumulators alternating over `stages`
+// stages of 128 columns starting at column `dcol` of a 512-column
+// allocation (one CTA per SM).
+__global__ void bank_pattern(long long *cyc, int nmma, int chain, int stages, int dcol, int *err) {
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __shared__ uint32_t taddr_s;
+    __shared__ __align__(8) unsigned long long done_bar;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    unsigned char *A = sm, *B = sm + 18432;
+    for (int i = tid; i < 8 * 2176 / 2; i += blockDim.x)
+        ((__half *)A)[i] = __float2half((float)((int)((i * 2654435761u) >> 25) - 64));
+    for (int i = tid; i < 128 * 32 / 2; i += blockDim.x)
+        ((__half *)B)[i] = __float2half((float)((int)((i * 40503u) >> 9 & 127) - 64));
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sa(&done_bar)));
+        asm volatile("fence.mbarrier_init.release.cluster;");
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(sa(&taddr_s)), "r"(512u));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    const uint32_t tm = taddr_s;
+    if (tid == 0) {
+        const long long t0 = clock64();
+        const uint32_t idesc = (1u << 4) | (1u << 15) | ((uint32_t)(128 >> 3) << 17) | ((128u >> 4) << 24);
+        const uint64_t a0 = desc(sa(A), 128, 128), b0 = desc(sa(B), 2048, 128);
+        uint32_t s = 0, k = 0, st = 0;
+        for (int i = 0; i < nmma; ++i) {
+            mma(tm + (uint32_t)dcol + st * 128u, a0 + (uint64_t)(s * (2176 >> 4)), b0, idesc, k ? 1u : 0u);
+            if (++s == 8) s = 0;
+            if (++k == (uint32_t)chain) {
+                k = 0;
+                if (++st == (uint32_t)stages) st = 0;
+            }
+        }
+        commit(&done_bar);
+        if (!wait_bounded(&done_bar, 0)) atomicExch(err, 1);
+        cyc[blockIdx.x] = clock64() - t0;
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tm), "r"(512u));
+}
+
+void run_bank_pattern(int sms, int chain, int stages, int dcol) {
+    const int nmma = 8192 / chain * chain, smem = 120 * 1024;  // one CTA per SM (512 TMEM columns)
+    cudaFuncSetAttribute(bank_pattern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    long long *cyc;
+    int *err;
+    cudaMalloc(&cyc, (size_t)sms * 8);
+    cudaMalloc(&err, 4);
+    cudaMemset(err, 0, 4);
+    bank_pattern<<<sms, 128, smem>>>(cyc, nmma, chain, stages, dcol, err);
+    bank_pattern<<<sms, 128, smem>>>(cyc, nmma, chain, stages, dcol, err);
+    long long *h = new long long[sms];
+    cudaMemcpy(h, cyc, (size_t)sms * 8, cudaMemcpyDeviceToHost);
+    long long mx = 0;
+    for (int i = 0; i < sms; ++i) mx = h[i] > mx ? h[i] : mx;
+    delete[] h;
+    int he = 0;
+    cudaMemcpy(&he, err, 4, cudaMemcpyDeviceToHost);
+    printf("bank pattern     chain %2d, %d stage(s) from column %3d: %6.1f SM cycles per MMA  err=%d %s\n",
+           chain, stages, dcol, (double)mx / nmma, he, cudaGetErrorString(cudaGetLastError()));
+    cudaFree(cyc);
+    cudaFree(err);
+}
+
+// The bank kernel's operand geometry at two CTAs per SM: A over a ring of
+// `aslots` slots of 2176 bytes (one per image row, advancing per MMA), B
+// (N = 128: two 64-template blocks) with its K halves `blbo` bytes apart and
+// its window moving by 1 KB per MMA over 17 positions; chains of 17 MMAs
+// alternating over two 128-column accumulators.
+__global__ void bank_geometry(long long *cyc, int nmma, int aslots, int blbo, int bmove, int *err) {
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __shared__ uint32_t taddr_s;
+    __shared__ __align__(8) unsigned long long done_bar;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int bBytes = blbo + 2048 + 17 * 1024;   // the moving window's reach, both K halves
+    unsigned char *B = sm, *A = sm + ((bBytes + 1023) / 1024) * 1024;
+    for (int i = tid; i < aslots * 2176 / 2; i += blockDim.x)
+        ((__half *)A)[i] = __float2half((float)((int)((i * 2654435761u) >> 25) - 64));
+    for (int i = tid; i < bBytes / 2; i += blockDim.x)
+        ((__half *)B)[i] = __float2half((float)((int)((i * 40503u) >> 9 & 127) - 64));
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sa(&done_bar)));
+        asm volatile("fence.mbarrier_init.release.cluster;");
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(sa(&taddr_s)), "r"(256u));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    const uint32_t tm = taddr_s;
+    if (tid == 0) {
+        const long long t0 = clock64();
+        const uint32_t idesc = (1u << 4) | (1u << 15) | ((uint32_t)(128 >> 3) << 17) | ((128u >> 4) << 24);
+        const uint64_t a0 = desc(sa(A), 128, 128), b0 = desc(sa(B), (uint32_t)blbo, 128);
+        uint32_t s = 0, k = 0, st = 0;
+        for (int i = 0; i < nmma; ++i) {
+            const uint32_t win = bmove ? (16u - k) * (1024u >> 4) : 0u;
+            mma(tm + st * 128u, a0 + (uint64_t)(s * (2176 >> 4)), b0 + win, idesc, k ? 1u : 0u);
+            if (++s == (uint32_t)aslots) s = 0;
+            if (++k == 17u) {
+                k = 0;
+                st ^= 1u;
+            }
+        }
+        commit(&done_bar);
+        if (!wait_bounded(&done_bar, 0)) atomicExch(err, 1);
+        cyc[blockIdx.x] = clock64() - t0;
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tm), "r"(256u));
+}
+
+void run_bank_geometry(int sms, int ctas, int aslots, int blbo, int bmove) {
+    const int blocks = sms * ctas, nmma = 17 * 480, smem = 110 * 1024;  // B reach + 32 A slots = 105 KB
+    cudaFuncSetAttribute(bank_geometry, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    long long *cyc;
+    int *err;
+    cudaMalloc(&cyc, (size_t)blocks * 8);
+    cudaMalloc(&err, 4);
+    cudaMemset(err, 0, 4);
+    bank_geometry<<<blocks, 128, smem>>>(cyc, nmma, aslots, blbo, bmove, err);
+    bank_geometry<<<blocks, 128, smem>>>(cyc, nmma, aslots, blbo, bmove, err);
+    long long *h = new long long[blocks];
+    cudaMemcpy(h, cyc, (size_t)blocks * 8, cudaMemcpyDeviceToHost);
+    long long mx = 0;
+    for (int i = 0; i < blocks; ++i) mx = h[i] > mx ? h[i] : mx;
+    delete[] h;
+    int he = 0;
+    cudaMemcpy(&he, err, 4, cudaMemcpyDeviceToHost);
+    printf("bank geometry    %d CTA(s)/SM, %2d A slots, B K halves %5d B apart%s: %6.1f SM cycles per MMA per CTA  err=%d %s\n",
+           ctas, aslots, blbo, bmove ? ", moving window" : "", (double)mx / nmma, he,
+           cudaGetErrorString(cudaGetLastError()));
+    cudaFree(cyc);
+    cudaFree(err);
+}
+
 // SM cycles of a try_wait on a phase that completed long before
 __global__ void wait_cost(long long *out) {
     __shared__ __align__(8) unsigned long long b;
@@ -333,6 +490,17 @@ int main() {
     run<4, 64, 5>("+ring bar.sync", sms, 1);
     run<7, 64, 0>("+wait/8", sms, 1);
     run<6, 64, 0>("2 issuers+wait", sms, 1);
+    run_bank_pattern(sms, 8192, 1, 0);
+    run_bank_pattern(sms, 8192, 1, 256);
+    run_bank_pattern(sms, 17, 1, 0);
+    run_bank_pattern(sms, 17, 2, 0);
+    run_bank_pattern(sms, 17, 2, 256);
+    run_bank_geometry(sms, 1, 8, 2048, 0);
+    run_bank_geometry(sms, 2, 8, 2048, 0);
+    run_bank_geometry(sms, 2, 32, 2048, 0);
+    run_bank_geometry(sms, 2, 32, 18432, 0);
+    run_bank_geometry(sms, 2, 32, 18432, 1);
+    run_bank_geometry(sms, 1, 32, 18432, 1);
     long long *w;
     cudaMalloc(&w, 16);
     wait_cost<<<1, 32>>>(w);
