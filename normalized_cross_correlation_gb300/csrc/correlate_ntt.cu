@@ -11,9 +11,10 @@
 //
 // Overlap-save tiling: tile (ty, tx) covers image rows ty*Vy .. +255 and
 // columns tx*Vx .. +255 (zeros beyond the image), with Vy = 257 - hT and
-// Vx = 257 - wT rounded down to a multiple of 16 (aligned tile columns).  Its cyclic correlation with the template equals the true
-// correlation at the Vy x Vx shifts whose windows do not wrap, and those
-// shifts tile the output map.  The values are centered (I - 128, T - 128),
+// Vx = 257 - wT rounded down to a multiple of 16 (aligned tile columns).
+// Its cyclic correlation with the template equals the true correlation at
+// the Vy x Vx shifts whose windows do not wrap, and those shifts tile the
+// output map.  The values are centered (I - 128, T - 128),
 // so |C| <= 2^14 * wT * hT, and
 //     SumIT = C + 128 * SumI + 128 * SumT - 16384 * N     (mod 2^32, exact).
 //
@@ -24,11 +25,12 @@
 //                        scaled by 1/65536, with Shoup companions (512 KB);
 //   ntt_corr_kernel      persistent, one CTA of 512 threads per SM: per tile
 //                        the pixels staged in shared memory (64 KB), the even
-//                        half (transform, product, inverse) into registers,
-//                        then the odd half, then the combination
-//                        y[r] = e[r] + o[r] (written back into the buffer)
-//                        and y[r+128] = e[r] - o[r], and the epilogue of each
-//                        half from the buffer, one output row per warp.
+//                        half (transform, product, inverse) parked in tensor
+//                        memory (tcgen05.st; no MMA), then the odd half, then
+//                        the combination y[r] = e[r] + w^-r o[r] (written
+//                        back into the buffer) and y[r+128] = e[r] - w^-r o[r]
+//                        (parked), and the epilogue of each half from the
+//                        buffer, one output row per warp.
 //                        Every step is a barrier-separated pass over the
 //                        136 KB shared buffer; no waits other than
 //                        __syncthreads.
