@@ -76,8 +76,7 @@ enum ncc_status_code {
  * row-major order so that every wait points at an earlier tile.  The
  * look-back state lives in a per-device workspace owned by the library: it
  * is allocated (cudaMalloc) on the first call on a device and whenever a
- * larger image needs more room -- make such a call before any stream
- * capture -- and reused afterwards without clearing.  Calls on different
+ * larger image needs more room, and reused afterwards without clearing.  Calls on different
  * streams are ordered through an event so they never share it concurrently.
  * The build kernel lets a kernel launched after it with programmatic stream
  * serialization start before it ends (ncc_match uses this); such a kernel
@@ -127,8 +126,8 @@ int ncc_sat_build_variant(const uint8_t *img, int W, int H, int64_t *S, int64_t 
  *   when ceil(W/128) * ceil(H/128) > 2729 tiles (4096x4096 fits; 8192x8192
  *   does not).
  * The first call on a device looks up the scratch array's device address
- * (cudaGetSymbolAddress); make it before any stream capture.  All calls on
- * a device share the array and each clears what it needs to start at zero;
+ * (cudaGetSymbolAddress, which allocates nothing).  All calls on a device
+ * share the array and each clears what it needs to start at zero;
  * calls whose kernels overlap on the GPU race on it, so order them (one
  * stream, or events).
  */

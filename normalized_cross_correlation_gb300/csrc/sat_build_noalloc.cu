@@ -13,8 +13,7 @@
 // Every GPU that loads the library holds one copy until the process exits.
 // Host code cannot use the array's name as a device address, so the first
 // call on each device looks the address up with cudaGetSymbolAddress (that
-// call allocates nothing) and caches it; make that first call before any
-// stream capture.  All calls on a device share the array and it keeps the
+// call allocates nothing) and caches it.  All calls on a device share the array and it keeps the
 // last call's contents, so each call clears the part the kernel needs to
 // start at zero; calls whose kernels overlap on the GPU (different streams,
 // no ordering between them) race on the array and must be ordered by the
