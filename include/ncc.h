@@ -239,10 +239,14 @@ int ncc_match(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
  * ordered on `stream`, then synchronizes it.
  *   img  host uint8 [H][W];  tmpl host uint8 [nT][hT][wT];
  *   out  host fp32 [nT][Oy][Ox].  Page-locked host memory makes the copies
- *   asynchronous and fast; pageable memory also works.  When `out` is
- *   page-locked memory the device can address, the kernels store the
- *   coefficients into it directly; otherwise they go to a device buffer that
- *   is copied back.
+ *   asynchronous and fast; pageable memory also works.
+ * A single template whose map has at least 8 MB of coefficients and goes to
+ * the dp4a kernel is correlated in up to 8 bands of output rows; each band
+ * is copied back on a non-blocking stream that the library keeps per device
+ * while the next band is correlated, and `stream` waits for those copies.
+ * Other maps: when `out` is page-locked memory the device can address, the
+ * kernels store the coefficients into it directly; otherwise they go to a
+ * device buffer that is copied back.
  * Device buffers come from a stream-ordered pool that the library keeps per
  * device (memory freed to it stays reserved for the next call) and go back
  * to it before return.  Returns the first failure among the steps, including

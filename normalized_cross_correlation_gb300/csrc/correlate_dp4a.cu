@@ -71,6 +71,8 @@ constexpr int kRowsPerThread = 8;
 constexpr int kWarps = 8;
 constexpr int kOutH = kWarps * kRowsPerThread;  // 64
 constexpr int kSmallRPT = 4;   // rows per thread of the 128 x 32 tiles
+static_assert(kCorrBandRows % kOutH == 0 && kCorrBandRows % (kWarps * kSmallRPT) == 0,
+              "row bands must consist of whole tiles");
 constexpr int kQuadMaxHT = 64; // narrow templates up to this height run four CTAs per SM
 constexpr int kThreads = kWarps * 32;
 constexpr int kMaxCtasPerSm = 3;   // resident CTAs per SM (launch bound)
@@ -152,6 +154,7 @@ struct KParams {
     int *status;
     int Ox, Oy;
     int lateWave;    // CTAs (linear id) that request their first table rows after the numerator
+    int tileRow0;    // first tile row of the launch (a band of output rows; 0 for the whole map)
     Geom g;
 };
 
@@ -256,8 +259,9 @@ corr_dp4a_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant
     const int epiBW = kNarrow ? kNarrowBW : g.epiBW, epiBuf = kNarrow ? kNarrowBuf : g.epiBuf;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // tile rows bottom-up: the table build writes its tables top-down, so
-    // the last rows it wrote -- still in L2 -- are read first
-    const int x0 = blockIdx.x * kOutW, y0 = (gridDim.y - 1 - blockIdx.y) * kTileH;
+    // the last rows it wrote -- still in L2 -- are read first; a launch over
+    // a band of output rows starts at tile row p.tileRow0
+    const int x0 = blockIdx.x * kOutW, y0 = (p.tileRow0 + (int)gridDim.y - 1 - (int)blockIdx.y) * kTileH;
     const int epiSteps = (min(kTileH, p.Oy - y0) + kEpiRowsPerStep - 1) / kEpiRowsPerStep;
     uint8_t *epi = smem + g.epiOff;
     // table-row segments of epilogue step t: rows y0+2t+h, buffers
@@ -818,7 +822,14 @@ cudaError_t corr_dp4a_launch(const CorrArgs &a, cudaStream_t stream) {
         tmaEpi = false;
     }
     if (small && !(tma && tmaEpi)) return cudaErrorNotSupported;  // the checks above exclude it
-    const dim3 grid((p.Ox + kOutW - 1) / kOutW, (p.Oy + tileH - 1) / tileH);
+    // a band of output rows [rowBegin, rowEnd): whole tiles only, so that no
+    // tile belongs to two bands (kCorrBandRows is a multiple of both heights)
+    const int rowEnd = a.rowEnd > 0 ? a.rowEnd : p.Oy;
+    if (a.rowBegin < 0 || a.rowBegin % tileH != 0 || rowEnd > p.Oy || a.rowBegin >= rowEnd ||
+        (rowEnd % tileH != 0 && rowEnd != p.Oy))
+        return cudaErrorInvalidValue;
+    p.tileRow0 = a.rowBegin / tileH;
+    const dim3 grid((p.Ox + kOutW - 1) / kOutW, (rowEnd + tileH - 1) / tileH - p.tileRow0);
     const dim3 block(kThreads);
     const size_t smem = (size_t)p.g.smemBytes;
     cudaError_t e;

@@ -57,6 +57,12 @@ constexpr long long kToeplitzMinOutputs = 4000000;
 constexpr long long kToeplitzMinDp4aSmall = 320;
 constexpr long long kNttMinDp4a = 320;
 constexpr long long kMaxN = 66051;  // wT*hT*255^2 < 2^32: SumIT fits uint32
+// The host-buffer path bands a single-template dp4a map from 8 MB of
+// coefficients on, into at most 8 bands (6 to 8 bands of a 66 MB map
+// measured best: 0.57 ms per call against 0.64 ms with the kernels storing
+// straight into page-locked memory).
+constexpr size_t kBandedMinBytes = 8u << 20;
+constexpr int kMaxBands = 8;
 
 int status_ptr(int **out) {
     int dev = 0;
@@ -144,34 +150,17 @@ int to_status(cudaError_t e) {
     return NCC_ERR_CUDA;
 }
 
-// Numerator + epilogue for nT templates, either coefficients or moments.
-// after_sat: the previous kernel on the stream is this library's SAT build
-// of img, so a single-template launch may overlap its tail.
-int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT, int nT,
-                  const int64_t *S, const int64_t *Q, float *out, int64_t *sumI,
-                  int64_t *sumI2, int64_t *sumIT, cudaStream_t stream, bool after_sat = false,
-                  bool direct = false) {
-    int *status = nullptr;
-    int rc = status_ptr(&status);
-    if (rc != NCC_OK) return rc;
-    const size_t Ox = (size_t)(W - wT + 1), Oy = (size_t)(H - hT + 1);
-    const size_t plane = Ox * Oy;
-    int path;
-    {
-        std::lock_guard<std::mutex> lock(g_mutex);
-        path = g_path;
-    }
-    if (!direct && nT > 1 && ncc::bank_tc_supported(W, H, wT, hT, nT)) {
-        ncc::BankArgs b{img, W, H, tmpl, wT, hT, nT, S, Q, out, sumI, sumI2, sumIT, status};
-        rc = to_status(ncc::bank_tc_launch(b, stream));
-        if (rc == NCC_OK) set_last_path(NCC_PATH_BANK);
-        return rc;
-    }
+// The numerator kernel for these sizes: NCC_PATH_BANK for a bank the
+// tensor-core bank kernel takes; otherwise the single-template kernel,
+// forced by `path` (ncc_debug_set_path) or picked automatically -- the
+// Toeplitz tensor-core product for templates whose numerator dominates, the
+// transform kernel for templates that product cannot take, dp4a for smaller
+// templates.  NCC_ERR_UNSUPPORTED when the forced or needed kernel cannot
+// take the sizes.
+int pick_kernel(int W, int H, int wT, int hT, int nT, int path, bool direct) {
+    if (!direct && nT > 1 && ncc::bank_tc_supported(W, H, wT, hT, nT)) return NCC_PATH_BANK;
     if (direct) path = NCC_PATH_DP4A;  // the direct moments exist on the dp4a kernel only
-    // The single-template kernel: forced, or automatically (for templates
-    // whose numerator dominates) the Toeplitz tensor-core product, the
-    // transform kernel for templates that product cannot take, and dp4a
-    // for smaller templates.
+    const long long plane = (long long)(W - wT + 1) * (H - hT + 1);
     const long long dp4aPerOutput = (long long)((wT + 3) / 4) * hT;
     int kernel = NCC_PATH_DP4A;
     if (path == NCC_PATH_TOEPLITZ || path == NCC_PATH_NTT) {
@@ -181,13 +170,45 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
         kernel = path;
     } else if (path == 0) {
         const bool tzOk = ncc::corr_toeplitz_supported(wT, hT);
-        const long long tzMin = (long long)plane >= kToeplitzMinOutputs ? kToeplitzMinDp4a : kToeplitzMinDp4aSmall;
+        const long long tzMin = plane >= kToeplitzMinOutputs ? kToeplitzMinDp4a : kToeplitzMinDp4aSmall;
         if (tzOk && dp4aPerOutput >= tzMin)
             kernel = NCC_PATH_TOEPLITZ;
         else if (!tzOk && ncc::corr_ntt_supported(wT, hT) && dp4aPerOutput >= kNttMinDp4a)
             kernel = NCC_PATH_NTT;
     }
     if (kernel == NCC_PATH_DP4A && !ncc::corr_dp4a_supported(wT, hT)) return NCC_ERR_UNSUPPORTED;
+    return kernel;
+}
+
+int current_path() {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    return g_path;
+}
+
+// Numerator + epilogue for nT templates, either coefficients or moments.
+// after_sat: the previous kernel on the stream is this library's SAT build
+// of img, so a single-template launch may overlap its tail.
+// rowBegin, rowEnd: only the output rows [rowBegin, rowEnd) (both 0: all),
+// on the dp4a kernel only (edges as CorrArgs requires).
+int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT, int hT, int nT,
+                  const int64_t *S, const int64_t *Q, float *out, int64_t *sumI,
+                  int64_t *sumI2, int64_t *sumIT, cudaStream_t stream, bool after_sat = false,
+                  bool direct = false, int rowBegin = 0, int rowEnd = 0) {
+    int *status = nullptr;
+    int rc = status_ptr(&status);
+    if (rc != NCC_OK) return rc;
+    const size_t plane = (size_t)(W - wT + 1) * (H - hT + 1);
+    const int path = current_path();
+    const int kernel = pick_kernel(W, H, wT, hT, nT, path, direct);
+    if (kernel < 0) return kernel;
+    const bool band = rowBegin != 0 || rowEnd != 0;
+    if (band && kernel != NCC_PATH_DP4A) return NCC_ERR_UNSUPPORTED;
+    if (kernel == NCC_PATH_BANK) {
+        ncc::BankArgs b{img, W, H, tmpl, wT, hT, nT, S, Q, out, sumI, sumI2, sumIT, status};
+        rc = to_status(ncc::bank_tc_launch(b, stream));
+        if (rc == NCC_OK) set_last_path(NCC_PATH_BANK);
+        return rc;
+    }
     int used = NCC_PATH_NONE;
     for (int t = 0; t < nT; ++t) {
         ncc::CorrArgs a;
@@ -203,6 +224,8 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
         a.status = status;
         a.overlap_prev = after_sat && t == 0;
         a.direct = direct;
+        a.rowBegin = rowBegin;
+        a.rowEnd = rowEnd;
         cudaError_t e = cudaErrorNotSupported;
         if (kernel == NCC_PATH_TOEPLITZ) {
             // plain stream order: behind the table build the early start
@@ -220,9 +243,28 @@ int run_correlate(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT,
             e = ncc::corr_dp4a_launch(a, stream);
             if (e == cudaSuccess) used = NCC_PATH_DP4A;
         }
-        if (e != cudaSuccess) return to_status(e);
+        if (e != cudaSuccess)
+            return band && e == cudaErrorInvalidValue ? NCC_ERR_INVALID_ARG : to_status(e);
     }
     set_last_path(used);
+    return NCC_OK;
+}
+
+// The host-buffer path's copy stream, one per device (non-blocking, kept for
+// the process): the coefficient bands go back to the host on it while the
+// correlation of the next band runs on the caller's stream.
+cudaStream_t g_copy_stream[kMaxDevices] = {};
+
+int copy_stream(cudaStream_t *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NCC_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_copy_stream[dev] &&
+        cudaStreamCreateWithFlags(&g_copy_stream[dev], cudaStreamNonBlocking) != cudaSuccess) {
+        g_copy_stream[dev] = nullptr;
+        return NCC_ERR_CUDA;
+    }
+    *out = g_copy_stream[dev];
     return NCC_OK;
 }
 
@@ -381,13 +423,19 @@ int ncc_match_host(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT
         return NCC_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const size_t n = (size_t)W * H, nt = (size_t)nT * wT * hT;
-    const size_t nout = (size_t)nT * (W - wT + 1) * (H - hT + 1);
-    // Page-locked output the device can address: the kernels store the
-    // coefficients straight into it over the host link, so there is no
-    // separate device-to-host copy after them.  Otherwise a device buffer
-    // and one copy.
+    const int Ox = W - wT + 1, Oy = H - hT + 1;
+    const size_t nout = (size_t)nT * Ox * Oy;
+    // A large single-template map on the dp4a kernel is correlated in bands
+    // of output rows, each copied back on the library's copy stream while
+    // the next band is correlated: the copy over the host link is the
+    // longest step (about 190 GB/s), and this hides all but the first
+    // band's correlation behind it.  Other maps: page-locked output that
+    // the device can address is written by the kernels directly over the
+    // link; otherwise a device buffer and one copy.
+    const bool banded = nT == 1 && nout * 4 >= kBandedMinBytes &&
+                        pick_kernel(W, H, wT, hT, nT, current_path(), false) == NCC_PATH_DP4A;
     float *direct = nullptr;
-    {
+    if (!banded) {
         cudaPointerAttributes pa;
         if (cudaPointerGetAttributes(&pa, out) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
             pa.devicePointer && (uintptr_t)pa.devicePointer % 4 == 0)
@@ -395,6 +443,8 @@ int ncc_match_host(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT
         else
             (void)cudaGetLastError();  // pageable memory: clear the query's error, if any
     }
+    cudaStream_t cs = nullptr;
+    if (banded && (rc = copy_stream(&cs)) != NCC_OK) return rc;
     // one device block: tables first (8-byte aligned), then out, image, templates
     const size_t outBytes = direct ? 0 : nout * 4;
     const size_t offQ = n * 8, offOut = 2 * n * 8, offImg = (offOut + outBytes + 255) / 256 * 256;
@@ -409,10 +459,47 @@ int ncc_match_host(const uint8_t *img, int W, int H, const uint8_t *tmpl, int wT
     if (cudaMemcpyAsync(dimg, img, n, cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemcpyAsync(dt, tmpl, nt, cudaMemcpyHostToDevice, st) != cudaSuccess)
         rc = NCC_ERR_CUDA;
-    if (rc == NCC_OK) rc = ncc_match(dimg, W, H, dt, wT, hT, nT, S, Q, dout, stream);
-    if (rc == NCC_OK && !direct &&
-        cudaMemcpyAsync(out, dout, nout * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        rc = NCC_ERR_CUDA;
+    if (!banded) {
+        if (rc == NCC_OK) rc = ncc_match(dimg, W, H, dt, wT, hT, nT, S, Q, dout, stream);
+        if (rc == NCC_OK && !direct &&
+            cudaMemcpyAsync(out, dout, nout * 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            rc = NCC_ERR_CUDA;
+    } else {
+        // at most kMaxBands bands of whole tiles, the bottom one first (the
+        // build writes the tables top-down, so its last rows are still in
+        // L2); the first band's launch overlaps the build's tail
+        const int per = (Oy + kMaxBands - 1) / kMaxBands;
+        const int bandRows = (per + ncc::kCorrBandRows - 1) / ncc::kCorrBandRows * ncc::kCorrBandRows;
+        const int nb = (Oy + bandRows - 1) / bandRows;
+        cudaEvent_t ev[kMaxBands + 1] = {};
+        int made = 0;
+        for (; made <= nb; ++made)
+            if (cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming) != cudaSuccess) break;
+        if (made <= nb) rc = NCC_ERR_CUDA;
+        if (rc == NCC_OK) rc = check_correlate(dimg, W, H, dt, wT, hT, nT, S, Q);
+        if (rc == NCC_OK) rc = ncc_sat_build(dimg, W, H, S, Q, stream);
+        // every band's kernel is enqueued before any copy: a copy into
+        // pageable memory returns only once it is done
+        int launched = 0;
+        for (int k = 0; k < nb && rc == NCC_OK; ++k, ++launched) {
+            const int b = nb - 1 - k, y0 = b * bandRows, y1 = y0 + bandRows < Oy ? y0 + bandRows : Oy;
+            rc = run_correlate(dimg, W, H, dt, wT, hT, 1, S, Q, dout, nullptr, nullptr, nullptr, st,
+                               k == 0, false, y0, y1);
+            if (rc == NCC_OK && cudaEventRecord(ev[k], st) != cudaSuccess) rc = NCC_ERR_CUDA;
+        }
+        for (int k = 0; k < launched && rc == NCC_OK; ++k) {
+            const int b = nb - 1 - k, y0 = b * bandRows, y1 = y0 + bandRows < Oy ? y0 + bandRows : Oy;
+            const size_t off = (size_t)y0 * Ox, cnt = (size_t)(y1 - y0) * Ox;
+            if (cudaStreamWaitEvent(cs, ev[k], 0) != cudaSuccess ||
+                cudaMemcpyAsync(out + off, dout + off, cnt * 4, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+                rc = NCC_ERR_CUDA;
+        }
+        // the caller's stream (and the buffers' release below) waits for the copies
+        if (made > nb && (cudaEventRecord(ev[nb], cs) != cudaSuccess ||
+                          cudaStreamWaitEvent(st, ev[nb], 0) != cudaSuccess) && rc == NCC_OK)
+            rc = NCC_ERR_CUDA;
+        for (int k = 0; k < made; ++k) cudaEventDestroy(ev[k]);
+    }
     cudaFreeAsync(d, st);
     const int rs = ncc_sync_status(stream);
     return rc != NCC_OK ? rc : rs;

@@ -177,7 +177,15 @@ struct CorrArgs {
     // Window moments from the staged image tile (sliding column sums and row
     // prefixes in shared memory) instead of from S and Q, which are unused.
     bool direct = false;
+    // Output rows [rowBegin, rowEnd) only (rowEnd 0: through the last row);
+    // dp4a kernel only.  rowBegin and, unless it is the map's last row,
+    // rowEnd must be multiples of kCorrBandRows.  The tables and the image
+    // are still the whole map's.
+    int rowBegin = 0, rowEnd = 0;
 };
+// Band edges for CorrArgs::rowBegin / rowEnd: a multiple of every tile
+// height of the dp4a kernel (32 and 64 rows).
+constexpr int kCorrBandRows = 64;
 // Multiprocessors of the current device (cached per device).
 int sm_count();
 bool corr_dp4a_supported(int wT, int hT);

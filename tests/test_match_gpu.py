@@ -107,6 +107,36 @@ def test_host_entry_point_matches_device_path(ncc, W, H, wT, hT, nT, pinned):
         np.testing.assert_array_equal(out.numpy(), r0)
 
 
+# Single-template maps of at least 8 MB on the dp4a kernel: the host-buffer
+# call correlates them in bands of whole tiles and copies each band back
+# while the next one is computed.  (W, H, wT, hT): 1085 output rows in 6
+# bands of 192 (the last ragged) on 128x32 tiles; 8 bands on 128x32 tiles;
+# 128x64 tiles (a 20-wide template on a map with enough tiles); the
+# plain-load path (a width that is not a multiple of 16).
+BANDED = [(2048, 1100, 16, 16), (1536, 1500, 13, 7), (2560, 1100, 20, 20), (2051, 1100, 16, 16)]
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("W,H,wT,hT", BANDED)
+def test_host_entry_point_in_bands(ncc, threads, W, H, wT, hT, pinned):
+    import torch
+    w = inputs.random_case(W * 3 + H + wT, W, H, wT, hT, nT=1, n_crops=1)
+    assert w.Ox * w.Oy * 4 >= 8 << 20
+    _, _, r0 = separate(ncc, to_dev(w.image), to_dev(w.templates))
+    img, T = torch.from_numpy(w.image), torch.from_numpy(w.templates)
+    out = torch.full((1, w.Oy, w.Ox), float("nan"), dtype=torch.float32)
+    if pinned:
+        img, T, out = img.pin_memory(), T.pin_memory(), out.pin_memory()
+    for _ in range(2):                        # the second call reuses the pooled buffers
+        out.fill_(float("nan"))
+        ncc.ncc_match_host(img, T, out)
+        assert ncc.lib().ncc_debug_last_path() == ncc.NCC_PATH_DP4A
+        np.testing.assert_array_equal(out.numpy(), r0)
+    if pinned and W == 2048:
+        ref = oracle.correlate(w.image, w.templates[0], threads=threads)
+        np.testing.assert_allclose(out.numpy()[0], ref, rtol=0, atol=TOL)
+
+
 def test_match_on_two_streams_at_once(ncc):
     """Two images matched on two streams with their calls interleaved: the
     builds share the library's look-back workspace (ordered through an
