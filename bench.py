@@ -90,9 +90,7 @@ NCU_TRAFFIC_BYTES = {
     ("sat_build", "ncc_4096_t16"): 229.4e6,
     ("sat_build", "large_8192_t64"): 1106.8e6,
     ("sat_build", "sat_8192"): 1106.8e6,
-    ("corr_dp4a", "ncc_4096_t16"): 337.7e6,
     ("bank_tc", "bank_2048_64x16"): 1104.4e6,
-    ("corr_dp4a_direct", "ncc_4096_t16"): 25.6e6,
     ("corr_toeplitz_tc", "large_8192_t64"): 1393.3e6,
     ("corr_ntt", "wide_4096_t128"): 338.2e6,
 }
