@@ -90,8 +90,8 @@ def f32(x):
 
 def fma32(a, b, c):
     """fma in float32: a*b + c formed exactly in float64 (all operands here
-    are integers below 2^26, so the product and the sum are exact there),
-    then rounded once."""
+    are integers and the product and the sum stay below 2^53, so both are
+    exact there), then rounded once."""
     return np.float32(np.float64(a) * np.float64(b) + np.float64(c))
 
 
