@@ -17,6 +17,8 @@ at the extremes that decide it.
   258 pixels): p2 = fl(SumI SumT), e2 = fma(SumI, SumT, -p2) (its exact
   error), num = fl(fma(N, SumIT, -p2) - e2), within a few units in the last
   place of the exact numerator, so the coefficient is within 1e-6.
+- The bounds behind the kernels' integer and fp32 widths and the transform
+  kernel's prime, each checked where it is tight.
 """
 import numpy as np
 import pytest
@@ -128,3 +130,44 @@ def test_bank_fp32_numerator_and_coefficient(wT, hT):
             r_f32 = np.float32(got) * np.float32(1.0 / np.sqrt(np.float64(vI))) * \
                 np.float32(1.0 / np.sqrt(np.float64(vT)))
             assert abs(float(r_f32) - r_exact) <= 1e-6
+
+
+def is_prime(n):
+    if n < 2:
+        return False
+    d = 2
+    while d * d <= n:
+        if n % d == 0:
+            return False
+        d += 1
+    return True
+
+
+def test_exactness_bounds_the_kernels_rely_on():
+    # table builder: a row's running sums in uint32 up to W = 66051 (the
+    # largest width whose row of 255s squares to less than 2^32); the
+    # look-back row words pack SumI in 25 bits and SumI2 in 32
+    assert 66051 * 255 ** 2 < 2 ** 32 <= 66052 * 255 ** 2
+    assert 66051 * 255 < 2 ** 25
+    # look-back words hold a table value in 57 bits: the largest Q entry of
+    # an image below 2^31 pixels
+    assert (2 ** 31 - 1) * 255 ** 2 < 2 ** 57
+    # dp4a numerator: SumIT in uint32 for templates up to 66051 pixels
+    assert 66051 * 255 ** 2 < 2 ** 32
+    # bank kernel: fp32 accumulation exact while a group has at most 258
+    # pixels (every partial sum an integer below 2^24)
+    assert 258 * 255 ** 2 < 2 ** 24 <= 259 * 255 ** 2
+    # Toeplitz kernel: centered products |(I-128)(T-128)| <= 2^14, groups of
+    # at most 1024 products stay within 2^24, where fp32 holds every integer
+    assert 128 * 128 == 2 ** 14 and 1024 * 2 ** 14 == 2 ** 24
+    assert float(np.float32(2 ** 24)) == 2 ** 24 and float(np.float32(2 ** 24 - 1)) == 2 ** 24 - 1
+    # transform kernel: p = 119 * 2^23 + 1 is prime, 3 generates its
+    # multiplicative group (so 256th roots of unity exist), and a centered
+    # correlation of up to 30000 pixels is recovered from its residue
+    p = 998244353
+    assert p == 119 * 2 ** 23 + 1 and is_prime(p)
+    assert all(pow(3, (p - 1) // q, p) != 1 for q in (2, 7, 17))     # p - 1 = 2^23 * 7 * 17
+    w256 = pow(3, (p - 1) // 256, p)
+    assert pow(w256, 256, p) == 1 and pow(w256, 128, p) == p - 1
+    assert 2 * 2 ** 14 * 30000 < p
+    assert 4 * p < 2 ** 32                                             # lazy residues in [0, 4p)
