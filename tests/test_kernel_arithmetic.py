@@ -17,8 +17,9 @@ at the extremes that decide it.
   258 pixels): p2 = fl(SumI SumT), e2 = fma(SumI, SumT, -p2) (its exact
   error), num = fl(fma(N, SumIT, -p2) - e2), within a few units in the last
   place of the exact numerator, so the coefficient is within 1e-6.
-- The bounds behind the kernels' integer and fp32 widths and the transform
-  kernel's prime, each checked where it is tight.
+- The bounds behind the kernels' integer and fp32 widths (the largest width
+  and group size checked one step past the limit too) and the transform
+  kernel's prime and roots of unity.
 """
 import numpy as np
 import pytest
