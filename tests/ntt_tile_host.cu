@@ -1,13 +1,16 @@
 // ntt_tile_host.cu -- runs the transform numerator's tile arithmetic
 // (normalized_cross_correlation_gb300/csrc/ntt_tile.cuh) on the host, pass by
 // pass for all 512 thread indices in turn (within a pass the threads touch
-// disjoint words, so the order is immaterial), and writes the centered
-// correlation of every non-wrapping shift.  Built and driven by
-// test_ntt_tile_host.py.
+// disjoint words, so the order is immaterial), combines the two halves in
+// place and reads the correlations back through the column swizzle as the
+// kernel does, and writes the centered correlation of every non-wrapping
+// shift.  Built and driven by test_ntt_tile_host.py.
 //
-//   ntt_tile_host wT hT in.bin out.bin
+//   ntt_tile_host wT hT in.bin out.bin [order]
 //     in.bin:  256 * 256 tile pixels (uint8, row-major), then hT * wT template
 //              pixels (uint8, row-major)
+//     order:   0, 1 or 2, the order in which the final combination visits
+//              the thread items (see below)
 //     out.bin: (257 - hT) * (257 - wT) int32, row-major: for shift (u, v),
 //              sum over (j, i) of (tile[u+j][v+i] - 128) * (T[j][i] - 128)
 #include <cstdio>
@@ -19,11 +22,13 @@
 using namespace ncc::ntt;
 
 int main(int argc, char **argv) {
-    if (argc != 5) {
-        std::fprintf(stderr, "usage: %s wT hT in.bin out.bin\n", argv[0]);
+    if (argc != 5 && argc != 6) {
+        std::fprintf(stderr, "usage: %s wT hT in.bin out.bin [order]\n", argv[0]);
         return 2;
     }
     const int wT = std::atoi(argv[1]), hT = std::atoi(argv[2]);
+    const int order = argc == 6 ? std::atoi(argv[5]) : 0;
+    if (order < 0 || order > 2) return 2;
     if (wT < 1 || hT < 1 || wT > kL || hT > kL) return 2;
     std::vector<uint8_t> img(kL * kL), tmpl((size_t)wT * hT);
     FILE *f = std::fopen(argv[3], "rb");
@@ -52,8 +57,24 @@ int main(int argc, char **argv) {
         for (int tid = 0; tid < kThreads; ++tid) cols_fwd1(tid, t);
         for (int tid = 0; tid < kThreads; ++tid) cols_spectrum(tid, t, H.data() + (size_t)half * kHalf * kL);
     }
-    // e: the even half's last pass, o: the odd half's times w^-r, per item
-    std::vector<uint32_t> e((size_t)kThreads * 4 * 16), o(e.size());
+    // The even half's last pass, per item (the kernel parks it in tensor
+    // memory).  Then, as the kernel does: the odd half's last pass combined
+    // with it in place -- y[r] = e + w^-r o written back into the buffer
+    // words that the same item's last pass read, y[r+128] = e - w^-r o
+    // parked -- and each half's correlations read back through the column
+    // swizzle.  The items run in the order `order` picks (0: thread-major,
+    // 1: item-major, 2: threads in reverse), so any item that read a word
+    // another item had already rewritten would change the result.
+    std::vector<uint32_t> e((size_t)kThreads * 4 * 16), parked(e.size());
+    auto items = [&](auto &&f) {
+        if (order == 1) {
+            for (int k = 0; k < 4; ++k)
+                for (int tid = 0; tid < kThreads; ++tid) f(tid, k);
+        } else {
+            for (int i = 0; i < kThreads; ++i)
+                for (int k = 0; k < 4; ++k) f(order == 2 ? kThreads - 1 - i : i, k);
+        }
+    };
     for (int half = 0; half < 2; ++half) {
         for (int tid = 0; tid < kThreads; ++tid)
             half ? rows_fwd1<true>(tid, t, loadI) : rows_fwd1<false>(tid, t, loadI);
@@ -62,27 +83,35 @@ int main(int argc, char **argv) {
         for (int tid = 0; tid < kThreads; ++tid) cols_mul(tid, t, H.data() + (size_t)half * kHalf * kL);
         for (int tid = 0; tid < kThreads; ++tid) cols_inv(tid, t);
         for (int tid = 0; tid < kThreads; ++tid) rows_inv1(tid, t);
-        for (int tid = 0; tid < kThreads; ++tid)
-            for (int k = 0; k < 4; ++k) {
-                uint32_t out[16];
-                rows_inv2(tid, k, t, out);
-                const int idx = tid + kThreads * k, r = idx >> 4;
-                for (int a = 0; a < 16; ++a)
-                    (half ? o : e)[(size_t)idx * 16 + a] = half ? mulw(out[a], t.rowFi[r]) : out[a];
+        items([&](int tid, int k) {
+            uint32_t out[16];
+            rows_inv2(tid, k, t, out);
+            const int idx = tid + kThreads * k, r = idx >> 4, n2 = idx & 15;
+            if (!half) {
+                for (int a = 0; a < 16; ++a) e[(size_t)idx * 16 + a] = out[a];
+                return;
             }
+            uint32_t *row = t.buf + r * kStride;
+            for (int a = 0; a < 16; ++a) {
+                const uint32_t ov = mulw(out[a], t.rowFi[r]), ev = red2(e[(size_t)idx * 16 + a]);
+                row[16 * a + (n2 ^ a)] = (uint32_t)centered(ev + ov);
+                parked[(size_t)idx * 16 + a] = (uint32_t)centered(ev - ov + kP2);
+            }
+        });
     }
     const int Vy = kL + 1 - hT, Vx = kL + 1 - wT;
     std::vector<int32_t> C((size_t)Vy * Vx);
-    for (int idx = 0; idx < kThreads * 4; ++idx) {
-        const int r = idx >> 4, n2 = idx & 15;
-        for (int a = 0; a < 16; ++a) {
-            const int c = 16 * a + n2;
-            if (c >= Vx) continue;
-            const uint32_t ev = red2(e[(size_t)idx * 16 + a]), ov = o[(size_t)idx * 16 + a];
-            if (r < Vy) C[(size_t)r * Vx + c] = centered(ev + ov);
-            if (r + kHalf < Vy) C[(size_t)(r + kHalf) * Vx + c] = centered(ev - ov + kP2);
-        }
-    }
+    auto read_half = [&](int u0) {
+        for (int rr = 0; rr < kHalf && u0 + rr < Vy; ++rr)
+            for (int xo = 0; xo < Vx; ++xo)
+                C[(size_t)(u0 + rr) * Vx + xo] = (int32_t)t.buf[rr * kStride + swz(xo)];
+    };
+    read_half(0);
+    items([&](int tid, int k) {           // the parked half back into the buffer
+        const int idx = tid + kThreads * k, r = idx >> 4, n2 = idx & 15;
+        for (int a = 0; a < 16; ++a) t.buf[r * kStride + 16 * a + (n2 ^ a)] = parked[(size_t)idx * 16 + a];
+    });
+    read_half(kHalf);
     f = std::fopen(argv[4], "wb");
     if (!f || std::fwrite(C.data(), 4, C.size(), f) != C.size()) return 4;
     std::fclose(f);

@@ -1,5 +1,6 @@
 """The transform numerator's tile arithmetic (ntt_tile.cuh), run on the host:
-every pass of a 256 x 256 tile for all 512 thread indices, against a
+every pass of a 256 x 256 tile for all 512 thread indices, the in-place
+combination of the two halves and the swizzled read-back, against a
 brute-force correlation of the centered values, bit for bit.
 
 The transforms are taken modulo the prime 998244353 with lazily reduced
@@ -48,11 +49,12 @@ def brute_force(tile, T):
     return C
 
 
-def run(exe, tmp_path, tile, T):
+def run(exe, tmp_path, tile, T, order=0):
     hT, wT = T.shape
     src, dst = tmp_path / "in.bin", tmp_path / "out.bin"
     src.write_bytes(tile.astype(np.uint8).tobytes() + T.astype(np.uint8).tobytes())
-    res = subprocess.run([exe, str(wT), str(hT), str(src), str(dst)], capture_output=True, text=True)
+    res = subprocess.run([exe, str(wT), str(hT), str(src), str(dst), str(order)],
+                         capture_output=True, text=True)
     assert res.returncode == 0, res.stderr
     return np.fromfile(dst, dtype=np.int32).reshape(257 - hT, 257 - wT)
 
@@ -75,3 +77,15 @@ def test_tile_correlation_at_the_bound(tile_exe, tmp_path, img_v, tmpl_v):
     np.testing.assert_array_equal(got, ref)
     assert np.abs(ref).max() >= 29929 * 16129       # 127 * 127 at (255, 255)
     assert np.abs(ref).max() < 998244353 // 2
+
+
+@pytest.mark.parametrize("order", [1, 2])
+@pytest.mark.parametrize("wT,hT", [(64, 64), (17, 9)])
+def test_in_place_combination_in_any_item_order(tile_exe, tmp_path, wT, hT, order):
+    """The halves are combined in place, each item rewriting only the words
+    its own last pass read: visiting the items in another order (item-major,
+    threads in reverse) gives the same correlations."""
+    rng = np.random.default_rng(wT * 31 + hT + order)
+    tile = rng.integers(0, 256, (256, 256), dtype=np.uint8)
+    T = rng.integers(0, 256, (hT, wT), dtype=np.uint8)
+    np.testing.assert_array_equal(run(tile_exe, tmp_path, tile, T, order), brute_force(tile, T))
